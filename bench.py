@@ -1,0 +1,370 @@
+"""Benchmark of the fused shared-prefix decode-attention launch on one GB300
+(or N independent replicas under torchrun, one per GPU: weak scaling).
+
+A step is one psattn_decode launch over one synthetic batch: the
+Llama-3-8B-shaped workload (64 prefix groups x 32 requests, prefix 2048
+tokens, suffix uniform in [64, 512], 32 query / 8 KV heads, head_dim 128,
+bf16, 16-token blocks).  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
+
+--impl reference times the CPU oracle (the only reference this method has),
+on a bounded sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = ("shared-prefix decode attention queries/s and achieved HBM GB/s "
+          "(% of roofline), 1 GB300")
+UNIT = "queries/s"
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_HBM_GBS = 6800.0
+
+DESCRIPTIONS = {
+    "llama8b": "Llama-3-8B attention shape: 64 prefix groups x 32 requests (2048), prefix 2048, "
+               "suffix U[64,512], 32 q / 8 kv heads, d 128, bf16, block 16",
+    "long_prefix": "8 groups x 100 requests, prefix U[1024,10240], suffix U[16,256], 32/8 heads, "
+                   "d 128, bf16, block 16",
+    "skewed": "1024 requests, Zipf(1.2) over 128 groups, 10% ungrouped, prefix LN(1500,0.8) "
+              "[64,8192], suffix LN(200,0.7) [1,2048], 32/8 heads, d 128, bf16",
+    "two_level": "4096 requests, level-1 prefix 4096 shared by all, level-2 1024 per 64 groups of "
+                 "64, suffix U[32,256], 3-partial merge, 32/8 heads, d 128, bf16",
+    "two_level_flat": "the two-level workload flattened to one 5120-token level per group",
+    "tiny_fp32": "2 groups x 8 requests, prefix 256, suffix U[1,64], 4/4 heads, d 64, fp32",
+}
+
+
+def _dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def _peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _traffic_record():
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    src = os.path.join(ROOT, "shared_prefix_kv_gb300", "csrc", "decode.cu")
+    path = os.path.join(ROOT, "profiles", "psattn_fused_decode_llama8b.md")
+    try:
+        text = open(path).read()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+        m_b = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+        if m_sha and m_b and m_sha.group(1) == sha:
+            return int(m_b.group(1))
+    except OSError:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.samples = []
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                self.samples.append((float(parts[0]), float(parts[1]), parts[3:7]))
+            except ValueError:
+                pass
+
+    def summary(self):
+        if not getattr(self, "samples", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in self.samples for i, v in enumerate(r)
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(s[0] for s in self.samples),
+                "sm_max_mhz": max(s[1] for s in self.samples), "reasons": reasons,
+                "samples": len(self.samples)}
+
+
+def _oracle_rate(p, budget_s: float, max_req=None):
+    """Queries/s of the CPU oracle over the first requests of the batch, run in
+    blocks until `budget_s` of wall time is spent."""
+    import oracle
+    order = np.arange(p.num_req)
+    done, t0 = 0, time.perf_counter()
+    block = 16
+    while done < p.num_req and (max_req is None or done < max_req):
+        req = order[done:done + block]
+        oracle.attention(p, req)
+        done += len(req)
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return done / dt, done, dt, oracle.max_threads()
+
+
+def run_reference(args, p):
+    """CPU oracle as the reference arm: each step attends a bounded sample of
+    requests of the same batch; value = requests / wall time."""
+    rank, world, _ = _dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    # calibrate so that warmup + steps stay within about a minute
+    rate, _, _, cores = _oracle_rate(p, 2.0, max_req=64)
+    per_step = max(1, min(p.num_req, int(60.0 * rate / max(1, args.steps + args.warmup))))
+    rng = np.random.default_rng(0)
+    for _ in range(args.warmup):
+        oracle.attention(p, rng.choice(p.num_req, per_step, replace=False))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.attention(p, rng.choice(p.num_req, per_step, replace=False))
+    dt = time.perf_counter() - t0
+    value = per_step * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": _config(args, p),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{per_step} random requests of the batch per step "
+                                   f"(all Hq heads, full prefix+suffix each)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _overrides(args):
+    return {} if args.groups is None else {"n_groups": args.groups}
+
+
+def _config(args, p):
+    desc = DESCRIPTIONS.get(args.workload, args.workload)
+    if args.groups is not None:
+        desc += f" (groups overridden to {args.groups})"
+    return {"workload": f"{args.workload}: {desc}",
+            "requests_per_gpu": p.num_req, "global_batch": p.num_req * args.gpus,
+            "parallelism": f"replicas x{args.gpus} (independent batches)",
+            "l2": "flushed (256 MiB write) between timed launches; KV working set > L2",
+            "seed": p.seed}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama8b", choices=sorted(DESCRIPTIONS))
+    ap.add_argument("--groups", type=int, default=None,
+                    help="override the number of prefix groups (smaller captures for profiling)")
+    ap.add_argument("--no-baselines", action="store_true",
+                    help="skip the CPU-oracle, no-dedup and end-to-end legs")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    rank, world, local = _dist_env()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        p = W.make(args.workload, poison=False, **_overrides(args))
+        return run_reference(args, p)
+
+    import torch
+    import shared_prefix_kv_gb300 as ps
+    from workloads.device import DeviceProblem, shape_of  # device upload helper (torch memory only)
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    # each rank gets its own independent batch (weak scaling)
+    p = W.make(args.workload, seed=None if rank == 0 else 1000 + rank, poison=False,
+               **_overrides(args))
+    d = DeviceProblem(p)
+    t_plan = time.perf_counter()
+    plan = d.plan()
+    t_plan = time.perf_counter() - t_plan
+    info = plan.info()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device="cuda")
+
+    def timed(pl, steps, warm):
+        for _ in range(warm):
+            d.decode(pl, stream)
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for a, b in ev:
+            flush.fill_(1)
+            a.record(stream)
+            d.decode(pl, stream)
+            b.record(stream)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        return [a.elapsed_time(b) for a, b in ev]
+
+    with ClockSampler(local) as clk:
+        times = timed(plan, args.steps, args.warmup)
+    rc, dflags = plan.status()
+    if rc != 0:
+        raise RuntimeError(f"device error word {dflags}")
+    ms = float(np.mean(times))
+    if dist:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = p.num_req * world / (ms * 1e-3)
+    alg_bytes = info["unique_kv_bytes"] + info["qo_bytes"]
+    peak, peak_kind = _peak_hbm()
+    achieved = alg_bytes / (ms * 1e-3) / 1e9
+    traffic = _traffic_record()
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if p.dtype == W.BF16 else "f32",
+        "data": "synthetic (seeded N(0,1) q/K/V, shuffled paged block tables)",
+        "config": _config(args, p),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "psattn_fused_decode",
+                     "algorithmic_bytes_per_launch": alg_bytes,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s"},
+        "achieved_hbm_gbs": achieved,
+        "pct_of_roofline": 100.0 * achieved / peak,
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+        "plan_ms": 1e3 * t_plan,
+        "ms_per_step_median": float(np.median(times)),
+    }
+
+    if not args.no_baselines:
+        # same kernel, prefix de-duplication disabled
+        nd = d.plan(ps.NO_DEDUP)
+        nd_times = timed(nd, max(20, args.steps // 4), 3)
+        nd_ms = float(np.mean(nd_times))
+        nd_info = nd.info()
+        line["no_dedup"] = {
+            "value": p.num_req * world / (nd_ms * 1e-3), "unit": UNIT, "ms_per_step": nd_ms,
+            "gbs_own_bytes": (nd_info["planned_kv_bytes"] + nd_info["qo_bytes"]) / (nd_ms * 1e-3) / 1e9,
+            "gbs_dedup_bytes": alg_bytes / (nd_ms * 1e-3) / 1e9}
+        nd.close()
+
+        # end to end through the public call with host buffers: H2D of the step's
+        # inputs (q, block table, group ids, lengths) from pinned memory, the
+        # launch, D2H of out and lse; the KV pool is device-resident cache state
+        hq = d.q.cpu().pin_memory()
+        host_in = [t.cpu().pin_memory() for t in (d.bt, d.gor, d.plen, d.slen)]
+        dev_in = [d.bt, d.gor, d.plen, d.slen]
+        h_out = torch.empty(d.out.shape, dtype=d.out.dtype).pin_memory()
+        h_lse = torch.empty(d.lse.shape, dtype=d.lse.dtype).pin_memory()
+        h2d = hq.numel() * hq.element_size() + sum(t.numel() * t.element_size() for t in host_in)
+        d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+
+        def e2e_step():
+            d.q.copy_(hq, non_blocking=True)
+            for dv, hv in zip(dev_in, host_in):
+                dv.copy_(hv, non_blocking=True)
+            d.decode(plan, stream)
+            h_out.copy_(d.out, non_blocking=True)
+            h_lse.copy_(d.lse, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        ne = max(20, args.steps // 4)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(ne):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e_ms = a.elapsed_time(b) / ne
+        if dist:
+            t = torch.tensor([e_ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        line["e2e"] = {"value": p.num_req * world / (e_ms * 1e-3), "unit": UNIT,
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": e_ms}
+        line["gpu_launches"] = args.steps
+
+        if rank == 0 and world == 1:
+            rate, n, dt, cores = _oracle_rate(p, 15.0)
+            line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                    "sample": f"first {n} requests of the batch ({dt:.1f} s "
+                                              f"wall, all heads, double precision)"}
+
+    plan.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,221 @@
+"""Parity of the fused CUDA decode (through the C ABI) with the CPU oracle.
+
+Element-wise on every output at sizes the oracle finishes in seconds (several
+tiles, ragged tails, NaN-poisoned unused slots), and on sampled requests at
+the full workload sizes in the benchmark's launch configuration.  Bounds:
+max abs error 1e-4 for fp32 inputs; 1e-2 on outputs and 1e-3 on LSE for bf16
+inputs (outputs compared after the kernel's bf16 rounding).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+def _lib():
+    import shared_prefix_kv_gb300 as ps  # fails loudly when the library is not built
+    return ps
+
+
+def _check(p, out, lse, requests=None):
+    from workloads.device import tolerances
+    o_ref, l_ref = oracle.attention(p, requests)
+    if requests is not None:
+        out, lse = out[requests], lse[requests]
+    t_out, t_lse = tolerances(p)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+    eo = np.abs(out - o_ref).max()
+    el = np.abs(lse - l_ref).max()
+    assert eo <= t_out, f"{p.name}: max |out - oracle| = {eo:.3g} > {t_out}"
+    assert el <= t_lse, f"{p.name}: max |lse - oracle| = {el:.3g} > {t_lse}"
+    return eo, el
+
+
+def _run(p, flags=0, launches=1):
+    from workloads.device import DeviceProblem
+    d = DeviceProblem(p)
+    with d.plan(flags) as pl:
+        for _ in range(launches):
+            d.decode(pl)
+        out, lse = d.result()
+        rc, dev_flags = pl.status()
+        assert rc == 0 and dev_flags == 0, (rc, dev_flags)
+    return out, lse
+
+
+SMALL = ["tiny_fp32", "llama8b", "long_prefix", "skewed", "two_level", "two_level_flat"]
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_parity_small(name):
+    _lib()
+    p = W.make(name, small=name != "tiny_fp32")
+    _check(p, *_run(p))
+
+
+@pytest.mark.parametrize("name", ["llama8b", "skewed", "two_level"])
+@pytest.mark.parametrize("flag", ["NO_DEDUP", "SIMT", "NO_TENSOR_PREFIX"])
+def test_parity_flags(name, flag):
+    ps = _lib()
+    p = W.make(name, small=True)
+    _check(p, *_run(p, getattr(ps, flag)))
+
+
+def test_parity_flatten_flag():
+    ps = _lib()
+    p = W.make("two_level", small=True)
+    _check(p, *_run(p, ps.FLATTEN))
+
+
+@pytest.mark.parametrize("seed", [100, 101, 102])
+def test_parity_more_seeds(seed):
+    _lib()
+    for name in ("llama8b", "skewed"):
+        p = W.make(name, seed=seed, small=True)
+        _check(p, *_run(p))
+
+
+def test_repeated_launches_reset_counters():
+    _lib()
+    p = W.make("skewed", small=True)
+    out, lse = _run(p, launches=4)
+    _check(p, out, lse)
+
+
+def _custom(Hq, Hkv, d, dtype, groups, parent, members, suffix, seed=0):
+    st = W.Structure(group_parent=parent, prefix_len=groups, group_of_req=members,
+                     suffix_len=suffix)
+    return W.materialize("custom", st, dtype=dtype, Hq=Hq, Hkv=Hkv, d=d, seed=seed)
+
+
+def test_edge_prefix_only_single_token_ungrouped():
+    _lib()
+    # suffix 0 (prefix only), one-token requests, ungrouped requests, a prefix of
+    # exactly one block, and one longer than a chunk
+    p = _custom(32, 8, 128, W.BF16, groups=[16, 1, 333], parent=None,
+                members=[0, 0, 1, 1, 2, 2, 2, -1, -1, 0],
+                suffix=[0, 1, 0, 17, 16, 0, 1, 1, 64, 33])
+    _check(p, *_run(p))
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(16, 2), (8, 4), (8, 8)])
+def test_edge_gqa_ratios_mma(Hq, Hkv):
+    _lib()
+    p = _custom(Hq, Hkv, 128, W.BF16, groups=[50, 200], parent=None,
+                members=[0, 1, 1, 0, -1, 1, 1, 1, 0], suffix=[3, 40, 0, 77, 5, 16, 9, 1, 130])
+    _check(p, *_run(p))
+
+
+@pytest.mark.parametrize("dtype,d", [(W.BF16, 64), (W.F32, 128), (W.F32, 64)])
+def test_edge_simt_shapes(dtype, d):
+    _lib()
+    p = _custom(8, 2, d, dtype, groups=[70, 33], parent=None,
+                members=[0, 0, 1, -1, 1, 0], suffix=[5, 0, 48, 3, 1, 100])
+    _check(p, *_run(p))
+
+
+def test_edge_three_level_chain():
+    _lib()
+    p = _custom(32, 8, 128, W.BF16, groups=[48, 20, 7, 100], parent=[-1, 0, 1, 0],
+                members=[2, 2, 1, 3, 3, 0, 2, -1], suffix=[4, 0, 9, 31, 2, 1, 50, 8])
+    _check(p, *_run(p))
+
+
+def test_edge_empty_batch():
+    ps = _lib()
+    from workloads.device import shape_of
+    sh = ps.make_shape(0, 0, 32, 8, 128, 16, 1, 64, ps.BF16, 0.088)
+    with ps.Plan(sh, np.zeros((0, 1), np.int32), np.zeros(0, np.int32), None, None,
+                 np.zeros(0, np.int32)) as pl:
+        x = torch.zeros(16, device="cuda", dtype=torch.bfloat16)
+        pl.decode(x, x, x, x, x, x, x, None)
+        assert pl.status() == (0, 0)
+
+
+def test_suffix_grows_without_replanning():
+    _lib()
+    from workloads.device import DeviceProblem
+    p = W.make("llama8b", small=True)
+    d = DeviceProblem(p)
+    with d.plan() as pl:
+        # grow every request whose last suffix block has a free slot by one token
+        grown = p.suffix_len.copy()
+        rng = np.random.default_rng(3)
+        for r in range(p.num_req):
+            s = int(p.suffix_len[r])
+            if s % 16:
+                col = int(np.count_nonzero(p.block_table[r] >= 0)) - 1
+                blk = p.block_table[r, col]
+                p.pool[blk, :, :, s % 16, :] = W.f32_to_bf16_bits(
+                    rng.standard_normal((2, p.num_kv_heads, p.head_dim)))
+                grown[r] = s + 1
+        p.suffix_len = grown
+        d2 = DeviceProblem(p)
+        d2.decode(pl)
+        out, lse = d2.result()
+        assert pl.status() == (0, 0)
+    _check(p, out, lse)
+
+
+def test_device_error_word_on_bad_block_id():
+    _lib()
+    from workloads.device import DeviceProblem
+    p = W.make("llama8b", small=True)
+    d = DeviceProblem(p)
+    with d.plan() as pl:
+        bt = p.block_table.copy()
+        bt[5, int(np.count_nonzero(bt[5] >= 0)) - 1] = p.num_pool_blocks + 1000
+        d.bt.copy_(torch.from_numpy(bt))
+        d.decode(pl)
+        rc, flags = pl.status()
+        assert rc == -7 and flags & 1
+        # the plan still works once the table is fixed
+        d.bt.copy_(torch.from_numpy(p.block_table))
+        d.decode(pl)
+        out, lse = d.result()
+        assert pl.status() == (0, 0)
+    _check(p, out, lse)
+
+
+def test_device_error_word_on_group_mismatch():
+    _lib()
+    from workloads.device import DeviceProblem
+    p = W.make("llama8b", small=True)
+    d = DeviceProblem(p)
+    with d.plan() as pl:
+        g = p.group_of_req.copy()
+        g[3] = (g[3] + 1) % p.num_groups
+        d.gor.copy_(torch.from_numpy(g))
+        d.decode(pl)
+        rc, flags = pl.status()
+        assert rc == -7 and flags & 2
+
+
+# ------------------------------------------------- full sizes, sampled outputs
+
+FULL = ["tiny_fp32", "llama8b", "long_prefix", "skewed", "two_level", "two_level_flat"]
+
+
+def _sample(p, n=40):
+    rng = np.random.default_rng(11)
+    picks = set(rng.choice(p.num_req, size=min(n, p.num_req), replace=False).tolist())
+    picks.add(int(np.argmax(p.suffix_len)))
+    picks.add(int(np.argmin(p.suffix_len)))
+    none = np.nonzero(p.group_of_req < 0)[0]
+    if none.size:
+        picks.add(int(none[0]))
+    return sorted(picks)
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_parity_full_size_sampled(name):
+    _lib()
+    p = W.make(name)
+    out, lse = _run(p)
+    _check(p, out, lse, _sample(p))
+    assert np.isfinite(out).all() and np.isfinite(lse).all()

@@ -1,0 +1,295 @@
+"""Bit-exact checks of the host planner (no GPU): every (request, KV head,
+token) is covered by exactly one partial, prefixes are read once per group,
+partial indices are a permutation, the tables are deterministic, and every
+malformed input is rejected with its status before any device work."""
+import re
+from collections import defaultdict
+
+import numpy as np
+import pytest
+
+import workloads as W
+import shared_prefix_kv_gb300 as ps
+
+ROOT_HEADER = __import__("os").path.join(__import__("os").path.dirname(__file__), "..",
+                                         "include", "psattn.h")
+
+
+def shape_of(p):
+    return ps.make_shape(p.num_req, p.num_groups, p.num_q_heads, p.num_kv_heads, p.head_dim,
+                         p.block_size, p.max_blocks_per_req, p.num_pool_blocks, p.dtype, p.scale)
+
+
+def host_plan(p, flags=0, sms=152, gpar="auto"):
+    gp = p.group_parent if gpar == "auto" else gpar
+    return ps.Plan(shape_of(p), p.block_table, p.group_of_req, gp, p.prefix_len, p.suffix_len,
+                   flags=flags, host_only_sms=sms)
+
+
+def tables(pl):
+    return dict(w=pl.export(ps.EXPORT_WARP_ITEMS).reshape(-1, 8),
+                d=pl.export(ps.EXPORT_DENSE_ITEMS).reshape(-1, 8),
+                req=pl.export(ps.EXPORT_REQ).reshape(-1, 8),
+                grp=pl.export(ps.EXPORT_GROUP).reshape(-1, 8),
+                mem=pl.export(ps.EXPORT_MEMBERS),
+                add=pl.export(ps.EXPORT_LEN_ADD))
+
+
+def item_span(t, it, p):
+    """Token range of an item, the way the kernel derives it from the tables."""
+    kind, kvh, seg, chunk = it[:4]
+    if kind == 0:
+        r = t["req"][seg]
+        ln, ch, n = int(p.suffix_len[seg]), r[3], r[4]
+    else:
+        g = t["grp"][seg]
+        ln, ch, n = int(p.prefix_len[seg]) + int(t["add"][seg]), g[1], g[2]
+    lo = chunk * ch
+    hi = ln if chunk == n - 1 else min(ln, lo + ch)
+    return lo, max(lo, hi)
+
+
+def item_members(t, it):
+    kind, _, seg, _, mem_off, nmem = it[:6]
+    if kind == 0:
+        return [int(seg)]
+    return [int(x) for x in t["mem"][mem_off:mem_off + nmem]]
+
+
+def expected_segments(p, flatten=False):
+    """(request -> list of (segment key, length)) from the problem itself."""
+    out = {}
+    for r in range(p.num_req):
+        ch = p.chain(r)
+        segs = []
+        if flatten and ch:
+            segs.append((("g", ch[-1]), sum(int(p.prefix_len[g]) for g in ch)))
+        else:
+            segs += [(("g", g), int(p.prefix_len[g])) for g in ch]
+        segs.append((("s", r), int(p.suffix_len[r])))
+        out[r] = [(k, n) for k, n in segs if n > 0]
+    return out
+
+
+CASES = ["tiny_fp32", "llama8b", "long_prefix", "skewed", "two_level", "two_level_flat"]
+
+
+@pytest.mark.parametrize("flags", [0, ps.NO_DEDUP, ps.SIMT])
+@pytest.mark.parametrize("name", CASES)
+def test_coverage_exact(name, flags):
+    p = W.make(name, small=True)
+    with host_plan(p, flags) as pl:
+        t = tables(pl)
+        Hkv = p.num_kv_heads
+        cover = defaultdict(list)   # (r, h, segkey) -> [(lo, hi)]
+        slots = defaultdict(list)   # (r, h) -> [slot_j]
+        for it in np.concatenate([t["w"], t["d"]]):
+            lo, hi = item_span(t, it, p)
+            key = ("s", int(it[2])) if it[0] == 0 else ("g", int(it[2]))
+            for r in item_members(t, it):
+                cover[(r, int(it[1]), key)].append((lo, hi))
+                slots[(r, int(it[1]))].append(int(it[6]))
+        segs = expected_segments(p)
+        for r in range(p.num_req):
+            nparts = int(t["req"][r][1])
+            for h in range(Hkv):
+                assert sorted(slots[(r, h)]) == list(range(nparts))
+                for key, n in segs[r]:
+                    spans = sorted(cover.pop((r, h, key)))
+                    pos = 0
+                    for lo, hi in spans:
+                        assert lo == pos
+                        pos = hi
+                    assert pos == n
+        assert not cover, f"items on segments a request does not own: {list(cover)[:3]}"
+
+
+@pytest.mark.parametrize("name", ["llama8b", "two_level", "skewed"])
+def test_prefix_read_once_per_group(name):
+    p = W.make(name, small=True)
+    for flags, per_item in [(0, 8 // (p.num_q_heads // p.num_kv_heads)), (ps.NO_DEDUP, 1)]:
+        with host_plan(p, flags) as pl:
+            t = tables(pl)
+            reads = defaultdict(int)
+            for it in t["w"]:
+                if it[0] == 1:
+                    lo, hi = item_span(t, it, p)
+                    reads[(int(it[2]), int(it[1]))] += hi - lo
+            for g in range(p.num_groups):
+                nmem = int(t["grp"][g][5])
+                if nmem == 0:
+                    continue
+                want = int(p.prefix_len[g]) * -(-nmem // per_item)
+                for h in range(p.num_kv_heads):
+                    assert reads[(g, h)] == want
+
+
+def test_group_tables_match_block_table():
+    p = W.make("two_level", small=True)
+    with host_plan(p) as pl:
+        t = tables(pl)
+        B = p.block_size
+        for r in range(p.num_req):
+            col = 0
+            for g in p.chain(r):
+                gi = t["grp"][g]
+                assert gi[0] == col
+                members = t["mem"][gi[4]:gi[4] + gi[5]]
+                assert r in members and gi[3] in members
+                n = -(-int(p.prefix_len[g]) // B)
+                assert np.array_equal(p.block_table[gi[3], col:col + n], p.block_table[r, col:col + n])
+                col += n
+            assert t["req"][r][2] == col
+            assert t["req"][r][5] == p.group_of_req[r]
+
+
+def test_deterministic_and_sorted():
+    p = W.make("skewed", small=True)
+    with host_plan(p) as a, host_plan(p) as b:
+        ta, tb = tables(a), tables(b)
+        for k in ta:
+            assert np.array_equal(ta[k], tb[k])
+        cost = ta["w"][:, 7]
+        assert (np.diff(cost) <= 0).all()
+
+
+def test_flatten_flag_equals_flattened_input():
+    a = W.make("two_level", small=True)
+    f = W.make("two_level_flat", small=True)
+    with host_plan(a, ps.FLATTEN) as pa, host_plan(f) as pf:
+        ia, ib = pa.info(), pf.info()
+        for k in ("warp_items", "partial_slots", "unique_kv_bytes", "planned_kv_bytes"):
+            assert ia[k] == ib[k], k
+        ta = tables(pa)
+        tf = tables(pf)
+        # the same (kind, kv head, chunk, member set, token span) multiset
+        def keyset(t, p):
+            return sorted((int(i[0]), int(i[1]), int(i[3]), tuple(sorted(item_members(t, i))),
+                           item_span(t, i, p)) for i in t["w"])
+        assert keyset(ta, a) == keyset(tf, f)
+
+
+def test_byte_accounting():
+    p = W.make("llama8b", small=True)
+    tb = 2 * p.num_kv_heads * p.head_dim * 2
+    uniq = (int(p.prefix_len.sum()) + int(p.suffix_len.sum())) * tb
+    with host_plan(p) as pl, host_plan(p, ps.NO_DEDUP) as nd:
+        assert pl.info()["unique_kv_bytes"] == uniq
+        chain_tok = sum(int(p.prefix_len[p.group_of_req[r]]) for r in range(p.num_req))
+        assert nd.info()["planned_kv_bytes"] == (chain_tok + int(p.suffix_len.sum())) * tb
+
+
+def test_plan_independent_of_call_order():
+    p = W.make("long_prefix", small=True)
+    with host_plan(p, sms=148) as a:
+        ta = tables(a)
+    with host_plan(p, sms=152) as b, host_plan(p, sms=148) as c:
+        tc = tables(c)
+    for k in ta:
+        assert np.array_equal(ta[k], tc[k])
+
+
+# ----------------------------------------------------------------- errors
+
+def _err(p, flags=0, **kw):
+    shape = kw.pop("shape", shape_of(p))
+    args = dict(block_table=p.block_table, group_of_req=p.group_of_req,
+                group_parent=p.group_parent, prefix_len=p.prefix_len, suffix_len=p.suffix_len)
+    args.update(kw)
+    with pytest.raises(ps.PsattnError) as e:
+        ps.psattn_plan_host(shape, args["block_table"], args["group_of_req"],
+                            args["group_parent"], args["prefix_len"], args["suffix_len"],
+                            flags, 152)
+    return e.value.status
+
+
+def test_error_block_oob():
+    p = W.make("tiny_fp32")
+    bt = p.block_table.copy()
+    last = int((bt[5] >= 0).sum()) - 1
+    bt[5, last] = p.num_pool_blocks + 7
+    assert _err(p, block_table=bt) == ps.ERR_BLOCK_OOB
+    bt[5, last] = -3
+    assert _err(p, block_table=bt) == ps.ERR_BLOCK_OOB
+
+
+def test_error_group_mismatch_and_no_dedup_accepts():
+    p = W.make("tiny_fp32")
+    bt = p.block_table.copy()
+    r = int(np.nonzero(p.group_of_req == 1)[0][2])
+    bt[r, 3] = bt[r, -1] if bt[r, -1] >= 0 else int(p.block_table.max())
+    assert _err(p, block_table=bt) == ps.ERR_GROUP_MISMATCH
+    h = ps.psattn_plan_host(shape_of(p), bt, p.group_of_req, None, p.prefix_len, p.suffix_len,
+                            ps.NO_DEDUP, 152)
+    ps.psattn_plan_destroy(h)
+
+
+def test_error_lengths_and_empty():
+    p = W.make("tiny_fp32")
+    s = p.suffix_len.copy(); s[0] = -1
+    assert _err(p, suffix_len=s) == ps.ERR_INVALID_ARG
+    pl = p.prefix_len.copy(); pl[1] = -5
+    assert _err(p, prefix_len=pl) == ps.ERR_INVALID_ARG
+    gor = p.group_of_req.copy(); gor[4] = -1
+    s = p.suffix_len.copy(); s[4] = 0
+    assert _err(p, group_of_req=gor, suffix_len=s) == ps.ERR_EMPTY_REQUEST
+    gor = p.group_of_req.copy(); gor[2] = p.num_groups
+    assert _err(p, group_of_req=gor) == ps.ERR_INVALID_ARG
+
+
+def test_error_table_too_narrow():
+    p = W.make("tiny_fp32")
+    sh = shape_of(p)
+    sh.max_blocks_per_req = p.max_blocks_per_req - 1
+    bt = np.ascontiguousarray(p.block_table[:, :-1])
+    assert _err(p, shape=sh, block_table=bt) == ps.ERR_INVALID_ARG
+
+
+def test_error_cycle():
+    p = W.make("two_level", small=True)
+    gp = p.group_parent.copy()
+    gp[0] = 2   # root now points into a child: cycle
+    assert _err(p, group_parent=gp) == ps.ERR_GROUP_CYCLE
+    gp = p.group_parent.copy(); gp[1] = 99
+    assert _err(p, group_parent=gp) == ps.ERR_GROUP_CYCLE
+
+
+def test_error_unsupported():
+    p = W.make("llama8b", small=True)
+    for field, val in [("block_size", 32), ("head_dim", 96), ("dtype", 7)]:
+        sh = shape_of(p)
+        setattr(sh, field, val)
+        assert _err(p, shape=sh) == ps.ERR_UNSUPPORTED
+    sh = shape_of(p); sh.num_q_heads = 12  # G = 1.5
+    assert _err(p, shape=sh) == ps.ERR_INVALID_ARG
+    sh = shape_of(p); sh.num_kv_heads = 2  # G = 16
+    assert _err(p, shape=sh) == ps.ERR_UNSUPPORTED
+
+
+def test_flatten_needs_whole_blocks():
+    p = W.make("two_level", small=True)
+    pl = p.prefix_len.copy(); pl[0] = 250   # root level not a whole number of blocks
+    assert _err(p, ps.FLATTEN, prefix_len=pl) in (ps.ERR_UNSUPPORTED, ps.ERR_GROUP_MISMATCH)
+
+
+def test_empty_batch_plans():
+    sh = ps.make_shape(0, 0, 32, 8, 128, 16, 1, 64, ps.BF16, 0.088)
+    h = ps.psattn_plan_host(sh, np.zeros((0, 1), np.int32), np.zeros(0, np.int32), None,
+                            None, np.zeros(0, np.int32), 0, 152)
+    info = ps.psattn_plan_info_get(h)
+    assert info["warp_items"] == 0 and info["partial_slots"] == 0
+    ps.psattn_plan_destroy(h)
+
+
+def test_status_strings():
+    for s in range(0, -10, -1):
+        assert ps.psattn_status_string(s) != "unknown status"
+
+
+def test_abi_exports_every_declared_symbol():
+    text = open(ROOT_HEADER).read()
+    declared = set(re.findall(r"^\s*(?:int|int64_t|void|const char\*)\s+(psattn_\w+)\s*\(",
+                              text, flags=re.M))
+    assert declared >= set(ps.EXPORTED_SYMBOLS)
+    for name in declared:
+        assert hasattr(ps._lib, name), name
