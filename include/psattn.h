@@ -167,6 +167,37 @@ int psattn_decode(psattn_plan_t plan, const void* q, const void* kv_pool,
                   const int32_t* prefix_len, const int32_t* suffix_len, void* out, float* lse,
                   psattn_stream_t stream);
 
+/*
+ * psattn_decode without any device allocation.  The paper has no counterpart:
+ * this exists for callers that cannot call cudaMalloc — a process whose device
+ * memory is already owned by another allocator (an engine that reserves
+ * nearly all of HBM for its KV-cache pool up front), or code on a
+ * latency-critical path where cudaMalloc/cudaFree are ruled out because they
+ * can synchronise the device.  The workspace psattn_plan would allocate lives
+ * instead in one fixed device array of PSATTN_NOALLOC_SCRATCH_BYTES inside the
+ * library, which every GPU that loads the library keeps until the process
+ * exits.
+ *
+ *  plan   a plan from psattn_plan_host (host tables only, no device memory;
+ *         pass the device's SM count) or from psattn_plan.
+ *  other arguments: as psattn_decode (device pointers, same layouts).
+ *
+ * The first call on a device looks up the array's device address with that
+ * device current; make that first call before any stream capture.  Every call
+ * clears the counters and tickets and uploads its plan's tables into the
+ * array, then runs the same fused kernel as psattn_decode, asynchronously on
+ * `stream`.  All calls share the array: calls whose launches overlap on the
+ * GPU race and give wrong results.  The kernel's error word is kept in the
+ * array and is not reported.  Returns INVALID_ARG (null or misaligned pointer),
+ * NOMEM (the plan's workspace exceeds PSATTN_NOALLOC_SCRATCH_BYTES; nothing is
+ * launched), CUDA.  Calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+#define PSATTN_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+int psattn_decode_noalloc(psattn_plan_t plan, const void* q, const void* kv_pool,
+                          const int32_t* block_table, const int32_t* group_of_req,
+                          const int32_t* prefix_len, const int32_t* suffix_len, void* out,
+                          float* lse, psattn_stream_t stream);
+
 /* Sizes and counts of a plan.  Returns INVALID_ARG on NULL. */
 int psattn_plan_info_get(psattn_plan_t plan, psattn_plan_info* info);
 

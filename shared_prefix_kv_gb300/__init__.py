@@ -179,6 +179,22 @@ def psattn_plan_destroy(plan: int) -> None:
     _lib.psattn_plan_destroy(plan)
 
 
+_lib.psattn_decode_noalloc.argtypes = [_vp] * 9 + [_vp]
+_lib.psattn_decode_noalloc.restype = ctypes.c_int
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
+
+
+def psattn_decode_noalloc(plan: int, q, kv_pool, block_table, group_of_req, prefix_len,
+                          suffix_len, out, lse, stream: int = 0) -> None:
+    """psattn_decode for callers that cannot allocate device memory: the
+    workspace lives in the library's fixed device array (see psattn.h)."""
+    rc = _lib.psattn_decode_noalloc(plan, _ptr(q), _ptr(kv_pool), _ptr(block_table),
+                                    _ptr(group_of_req), _ptr(prefix_len), _ptr(suffix_len),
+                                    _ptr(out), _ptr(lse), stream or None)
+    if rc != OK:
+        raise PsattnError(rc, "psattn_decode_noalloc")
+
+
 class Plan:
     """Owns a plan handle; ``close()`` (or the context manager) frees it."""
 

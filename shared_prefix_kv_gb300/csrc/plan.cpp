@@ -384,6 +384,10 @@ int upload(psattn_plan_s* p, cudaStream_t stream) {
 
 }  // namespace
 
+const psattn::HostPlan* psattn_internal_host_plan(psattn_plan_t plan) {
+  return plan ? &plan->hp : nullptr;
+}
+
 extern "C" {
 
 int psattn_plan_host(const psattn_shape* shape, const int32_t* block_table,

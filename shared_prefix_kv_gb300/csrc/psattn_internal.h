@@ -98,6 +98,9 @@ struct DevPlan {
 
 }  // namespace psattn
 
+// Host tables of a plan (plan.cpp), for the library's other translation units.
+const psattn::HostPlan* psattn_internal_host_plan(psattn_plan_t plan);
+
 // Implemented in decode.cu.
 int psattn_launch_decode(const psattn::HostPlan& hp, const psattn::DevPlan& dp, const void* q,
                          const void* kv_pool, const int32_t* block_table,
