@@ -27,6 +27,8 @@ def _flags(verbose_ptxas: bool):
          "-I", os.path.join(ROOT, "include"), "-I", CSRC, *ARCH]
     if verbose_ptxas:
         f += ["-Xptxas", "-v"]
+    # extra nvcc flags (tuning defines such as -DPSATTN_PREFETCH_BLOCKS=4)
+    f += os.environ.get("PSATTN_NVCC_EXTRA", "").split()
     return f
 
 
@@ -46,7 +48,7 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
         path = os.path.join(CSRC, src)
         obj = os.path.join(OUT, src + ".o")
         objs.append(obj)
-        if force or verbose_ptxas or _stale(obj, [path, *headers]):
+        if force or verbose_ptxas or os.environ.get("PSATTN_NVCC_EXTRA") or _stale(obj, [path, *headers]):
             lang = ["-x", "cu"] if src.endswith(".cu") else ["-x", "c++"]
             jobs.append([_nvcc(), *_flags(verbose_ptxas), *lang, "-c", path, "-o", obj])
 

@@ -22,9 +22,12 @@
 // a ticket; whoever takes the last ticket merges.  Nothing ever waits on
 // another item.  The merger resets the ticket, and the last CTA to leave
 // resets the work counters, so consecutive launches need no memset.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <cstring>
 
 #include "psattn_internal.h"
 
@@ -37,6 +40,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kThreads = kWarpsPerCta * 32;
 
 struct Params {
+  CUtensorMap kv_map;  // the pool as [num_blocks * 2 * Hkv * 16 rows][d] bf16, 128B swizzle
   DevPlan dp;
   const void* q;
   const void* pool;
@@ -146,33 +150,56 @@ __device__ __forceinline__ Span resolve(const Params& P, const Item& it) {
   return s;
 }
 
-// Block ids of a span, 32 at a time in a register of every lane; returns the
-// physical id of local block bi (warp-uniform), or -1 when it is out of range.
-struct BlockIds {
-  int cache, base;
-  __device__ __forceinline__ BlockIds() : cache(-1), base(-64) {}
-  __device__ __forceinline__ int get(const Params& P, const Span& s, int bi, int nb, int lane) {
-    if (bi - base >= 32 || bi < base) {
-      base = bi;
-      int id = -1;
-      const int b = bi + lane;
-      if (b < nb) {
-        const int col = s.col0 + b;
-        if (col >= P.maxb) {
-          raise(P, kErrColumn);
-        } else {
-          id = __ldg(&P.bt[(size_t)s.rep * P.maxb + col]);
-          if (id < 0 || id >= P.nblocks) {
-            raise(P, kErrBlockOob);
-            id = -1;
-          }
-        }
-      }
-      cache = id;
+// Block ids of a span in a sliding 64-entry window: lane i holds the ids of
+// local blocks base + i and base + 32 + i.  Out-of-range columns or ids raise
+// the error word and read as -1 (the block is skipped, never dereferenced).
+struct BlockWin {
+  int lo, hi, base;
+  __device__ __forceinline__ int fetch(const Params& P, const Span& s, int b, int nb) const {
+    if (b >= nb) return -1;
+    const int col = s.col0 + b;
+    if (col >= P.maxb) {
+      raise(P, kErrColumn);
+      return -1;
     }
-    return __shfl_sync(0xffffffffu, cache, bi - base);
+    const int id = __ldg(&P.bt[(size_t)s.rep * P.maxb + col]);
+    if (id < 0 || id >= P.nblocks) {
+      raise(P, kErrBlockOob);
+      return -1;
+    }
+    return id;
+  }
+  __device__ __forceinline__ void init(const Params& P, const Span& s, int nb, int lane) {
+    base = 0;
+    lo = fetch(P, s, lane, nb);
+    hi = fetch(P, s, 32 + lane, nb);
+  }
+  // keep local block bi in [base, base + 32) so that bi + d stays in the window for d < 32
+  __device__ __forceinline__ void advance(const Params& P, const Span& s, int bi, int nb, int lane) {
+    if (bi >= base + 32) {
+      lo = hi;
+      base += 32;
+      hi = fetch(P, s, base + 32 + lane, nb);
+    }
+  }
+  // warp-uniform b in [base, base + 64)
+  __device__ __forceinline__ int get(int b) const {
+    const int v = (b - base < 32) ? lo : hi;
+    return __shfl_sync(0xffffffffu, v, (b - base) & 31);
   }
 };
+
+// Bulk prefetch of one (block, K|V, head) tile into L2 (no register or shared
+// memory cost); keeps several tiles per warp in flight ahead of the loads.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+#ifndef PSATTN_PREFETCH_BLOCKS
+#define PSATTN_PREFETCH_BLOCKS 3
+#endif
+constexpr int kPrefetchBlocks = PSATTN_PREFETCH_BLOCKS;  // prefetch distance in blocks (0: off)
+static_assert(kPrefetchBlocks >= 0 && kPrefetchBlocks < 32, "prefetch distance");
 
 // ------------------------------------------------------------------- merging
 
@@ -350,9 +377,18 @@ __device__ __forceinline__ void mma_item(const Params& P, const Item& it, int la
   const int nb = (s.t1 > s.t0) ? (s.t1 - s.t0 + kBlockSize - 1) / kBlockSize : 0;
   const size_t head_stride = (size_t)kBlockSize * D;  // elements of one (block, K|V, head) tile
   const __nv_bfloat16* pool = reinterpret_cast<const __nv_bfloat16*>(P.pool);
-  BlockIds ids;
+  const uint32_t tile_bytes = (uint32_t)(head_stride * sizeof(__nv_bfloat16));
+  BlockWin win;
+  win.init(P, s, nb, lane);
+  auto prefetch_block = [&](int id) {
+    prefetch_l2(pool + ((size_t)id * 2 * P.Hkv + h) * head_stride, tile_bytes);
+    prefetch_l2(pool + (((size_t)id * 2 + 1) * P.Hkv + h) * head_stride, tile_bytes);
+  };
+  // lane i already holds the id of local block i: no shuffle (a full-mask
+  // shuffle here would be reached by only some lanes)
+  if (lane < kPrefetchBlocks && win.lo >= 0) prefetch_block(win.lo);
   uint4 kr[2][4];
-  int id_next = nb > 0 ? ids.get(P, s, 0, nb, lane) : -1;
+  int id_next = nb > 0 ? win.get(0) : -1;
   auto load_k = [&](int id) {
     const __nv_bfloat16* kb = pool + ((size_t)id * 2 * P.Hkv + h) * head_stride;
 #pragma unroll
@@ -363,6 +399,11 @@ __device__ __forceinline__ void mma_item(const Params& P, const Item& it, int la
   if (id_next >= 0) load_k(id_next);
 
   for (int bi = 0; bi < nb; ++bi) {
+    win.advance(P, s, bi, nb, lane);
+    if (kPrefetchBlocks > 0 && bi + kPrefetchBlocks < nb) {
+      const int pid = win.get(bi + kPrefetchBlocks);
+      if (lane == 0 && pid >= 0) prefetch_block(pid);
+    }
     const int id = id_next;
     const int nvalid = min(kBlockSize, s.t1 - (s.t0 + bi * kBlockSize));
     uint4 vr[4][2];
@@ -385,7 +426,7 @@ __device__ __forceinline__ void mma_item(const Params& P, const Item& it, int la
       }
     }
     if (bi + 1 < nb) {
-      id_next = ids.get(P, s, bi + 1, nb, lane);
+      id_next = win.get(bi + 1);
       if (id_next >= 0) load_k(id_next);
     }
     if (id < 0) continue;
@@ -520,9 +561,23 @@ __device__ __forceinline__ void simt_item(const Params& P, const Item& it, int l
   const int nb = (s.t1 > s.t0) ? (s.t1 - s.t0 + kBlockSize - 1) / kBlockSize : 0;
   const size_t head_stride = (size_t)kBlockSize * D;
   const T* pool = reinterpret_cast<const T*>(P.pool);
-  BlockIds ids;
+  const uint32_t tile_bytes = (uint32_t)(head_stride * sizeof(T));
+  BlockWin win;
+  win.init(P, s, nb, lane);
+  if (lane < kPrefetchBlocks && win.lo >= 0) {
+    prefetch_l2(pool + ((size_t)win.lo * 2 * P.Hkv + h) * head_stride, tile_bytes);
+    prefetch_l2(pool + (((size_t)win.lo * 2 + 1) * P.Hkv + h) * head_stride, tile_bytes);
+  }
   for (int bi = 0; bi < nb; ++bi) {
-    const int id = ids.get(P, s, bi, nb, lane);
+    win.advance(P, s, bi, nb, lane);
+    if (kPrefetchBlocks > 0 && bi + kPrefetchBlocks < nb) {
+      const int pid = win.get(bi + kPrefetchBlocks);
+      if (lane == 0 && pid >= 0) {
+        prefetch_l2(pool + ((size_t)pid * 2 * P.Hkv + h) * head_stride, tile_bytes);
+        prefetch_l2(pool + (((size_t)pid * 2 + 1) * P.Hkv + h) * head_stride, tile_bytes);
+      }
+    }
+    const int id = win.get(bi);
     if (id < 0) continue;
     const int nvalid = min(kBlockSize, s.t1 - (s.t0 + bi * kBlockSize));
     const T* kb = pool + ((size_t)id * 2 * P.Hkv + h) * head_stride;
@@ -586,6 +641,530 @@ __device__ __forceinline__ void simt_item(const Params& P, const Item& it, int l
   finish_item<T, D>(P, it, own, lane);
 }
 
+// ------------------------------------ tensor-core prefix tile (tcgen05 + TMA)
+//
+// A dense item is (group, KV head, chunk of the group's level, up to 128/G
+// members): 128 rows of q (member x q head of the KV head; padding rows are
+// zero) against the chunk's K/V, read once for all rows (the prefix partial as
+// a matrix product, BatchLLM section 2.2).  Warps 0-3 of the CTA run it: thread
+// 0 issues the TMA copies and the tcgen05 MMAs, and all 128 threads do the
+// softmax and the epilogue, thread t owning row t (= TMEM lane t).
+//
+// Per 128-token tile j (stage j & 1 of a double-buffered K/V ring):
+//   TMA: 8 paged blocks x {K, V} x 2 halves of d, 128B-swizzled boxes of
+//        16 rows x 64 columns straight from the pool (tensor map over the pool
+//        as [rows = block*2*Hkv*16][d]);
+//   S = Q K^T   tcgen05.mma kind::f16, M 128, N 128, K 128 (8 steps), fp32 in
+//               TMEM columns [0, 128); Q and K are K-major;
+//   softmax     tcgen05.ld of S, running max m in log2 units, raised only when
+//               the tile max exceeds it by more than 8 (then O is rescaled in
+//               TMEM), P = 2^(s - m) as bf16 into a 128B-swizzled K-major tile;
+//   O += P V    tcgen05.mma, N 128 (d), K 128 tokens, V as the MN-major B
+//               operand, fp32 in TMEM columns [128, 256).
+// Every wait is bounded; a timeout raises the error word and ends the dense
+// work of the CTA without touching the rest.
+
+constexpr int kTileTok = 128;
+constexpr uint32_t kTileBytes = 128 * 128 * 2;          // one 128 x 128 bf16 operand tile
+constexpr uint32_t kHalfBytes = kTileBytes / 2;         // one 64-column half (K atom)
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = kTileBytes;                  // 2 stages
+constexpr uint32_t kOffV = 3 * kTileBytes;              // 2 stages
+constexpr uint32_t kOffP = 5 * kTileBytes;
+constexpr uint32_t kOffIds = 6 * kTileBytes;            // block ids of the chunk
+constexpr int kMaxDenseBlocks = 512;                    // chunk <= 8192 tokens
+constexpr uint32_t kOffBar = kOffIds + kMaxDenseBlocks * 4;
+constexpr uint32_t kOffMisc = kOffBar + 64;
+constexpr uint32_t kDenseSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
+constexpr uint32_t kTmemCols = 256;
+constexpr float kRescaleThreshold = 8.0f;               // log2 units
+constexpr uint64_t kWaitLimitNs = 2000000000ull;        // 2 s per wait
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for phase `parity` of an mbarrier; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// named barrier 1 over the 128 threads of warps 0-3
+__device__ __forceinline__ void group_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// barrier that also ORs a flag over the 128 threads (uniform abort decisions)
+__device__ __forceinline__ bool group_sync_or(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n bar.red.or.pred po, 1, 128, pi;\n"
+      " selp.u32 %0, 1, 0, po;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
+          taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (start, leading and stride
+// byte offsets in 16-byte units; bits 46-48 fixed 0b001; layout 2 = SW128).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, M = 128, N = 128;
+// b_mn_major selects an MN-major B operand.
+__host__ __device__ constexpr uint32_t idesc_bf16_m128_n128(bool b_mn_major) {
+  return (1u << 4)            // D format fp32
+         | (1u << 7)          // A format bf16
+         | (1u << 10)         // B format bf16
+         | ((b_mn_major ? 1u : 0u) << 16)
+         | ((128u >> 3) << 17)  // N / 8
+         | ((128u >> 4) << 24); // M / 16
+}
+
+struct DenseState {
+  uint8_t* smem;      // 1024-aligned
+  uint32_t sbase;     // its shared-space address
+  uint32_t tmem;      // TMEM base (lane 0, column of S)
+  uint32_t ph_kv0, ph_kv1, ph_s, ph_o;
+};
+
+__device__ __forceinline__ uint32_t bar_kv(const DenseState& d, int st) {
+  return d.sbase + kOffBar + 8u * st;
+}
+__device__ __forceinline__ uint32_t bar_s(const DenseState& d) { return d.sbase + kOffBar + 16; }
+__device__ __forceinline__ uint32_t bar_o(const DenseState& d) { return d.sbase + kOffBar + 24; }
+
+// TMA of tile j of the chunk into stage j & 1 (thread 0 only).
+__device__ __forceinline__ void issue_tile(const Params& P, const DenseState& d, int j, int nb,
+                                           int h) {
+  const int st = j & 1;
+  const int* ids = reinterpret_cast<const int*>(d.smem + kOffIds);
+  const int b0 = j * (kTileTok / kBlockSize), b1 = min(nb, b0 + kTileTok / kBlockSize);
+  uint32_t bytes = 0;
+  for (int b = b0; b < b1; ++b)
+    if (ids[b] >= 0) bytes += 4u * kBlockSize * 64u * 2u;  // K and V x two 16 x 64 halves
+  const uint32_t bar = bar_kv(d, st);
+  mbar_expect_tx(bar, bytes);
+  const uint32_t ks = d.sbase + kOffK + st * kTileBytes, vs = d.sbase + kOffV + st * kTileBytes;
+  for (int b = b0; b < b1; ++b) {
+    const int id = ids[b];
+    if (id < 0) continue;
+    const int rk = ((id * 2 + 0) * P.Hkv + h) * kBlockSize;
+    const int rv = ((id * 2 + 1) * P.Hkv + h) * kBlockSize;
+    const uint32_t off = (uint32_t)(b - b0) * (kBlockSize * 128u);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      tma_load_2d(ks + half * kHalfBytes + off, &P.kv_map, half * 64, rk, bar);
+      tma_load_2d(vs + half * kHalfBytes + off, &P.kv_map, half * 64, rv, bar);
+    }
+  }
+}
+
+// One dense item.  Returns false when a wait timed out (uniform over the group).
+__device__ bool dense_item(const Params& P, DenseState& d, const Item& it) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = P.G, h = it.kvh;
+  const Span s = resolve(P, it);
+  const int nrows = s.nmem * G;
+  int ntok = s.t1 - s.t0;
+  if (ntok > kMaxDenseBlocks * kBlockSize) {  // device lengths beyond what was planned
+    if (tid == 0) raise(P, kErrColumn);
+    ntok = kMaxDenseBlocks * kBlockSize;
+  }
+  const int nb = (ntok + kBlockSize - 1) / kBlockSize;
+  const int ntiles = (ntok + kTileTok - 1) / kTileTok;
+
+  // block ids of the chunk -> shared memory (bad ids raise the error word, read -1)
+  int* ids = reinterpret_cast<int*>(d.smem + kOffIds);
+  for (int b = tid; b < nb; b += 128) {
+    int id = -1;
+    const int col = s.col0 + b;
+    if (col >= P.maxb) {
+      raise(P, kErrColumn);
+    } else {
+      id = __ldg(&P.bt[(size_t)s.rep * P.maxb + col]);
+      if (id < 0 || id >= P.nblocks) {
+        raise(P, kErrBlockOob);
+        id = -1;
+      }
+    }
+    ids[b] = id;
+  }
+  // Q tile, K-major, 128B swizzle: 16-byte chunk c of row t at
+  // atom (c / 8), row t, position (c % 8) ^ (t % 8)
+  {
+    uint8_t* qs = d.smem + kOffQ;
+    const __nv_bfloat16* qp = nullptr;
+    if (tid < nrows) {
+      const int r = member_req(P, it, tid / G);
+      qp = reinterpret_cast<const __nv_bfloat16*>(P.q) + ((size_t)r * P.Hq + h * G + tid % G) * 128;
+    }
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const uint4 w = qp ? __ldg(reinterpret_cast<const uint4*>(qp + 8 * c)) : make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(qs + (c >> 3) * kHalfBytes + tid * 128 + (((c & 7) ^ (tid & 7)) << 4)) = w;
+    }
+  }
+  fence_proxy_async();
+  group_sync();
+  if (tid == 0 && ntiles > 0) issue_tile(P, d, 0, nb, h);
+
+  const uint32_t trow = d.tmem + ((uint32_t)(warp * 32) << 16);
+  const uint32_t idesc_s = idesc_bf16_m128_n128(false), idesc_o = idesc_bf16_m128_n128(true);
+  float m_run = -INFINITY, l_run = 0.f;
+  for (int j = 0; j < ntiles; ++j) {
+    const int st = j & 1;
+    const int tile_valid = min(kTileTok, ntok - j * kTileTok);
+    bool to = !mbar_wait(bar_kv(d, st), st ? d.ph_kv1 : d.ph_kv0);
+    if (st) d.ph_kv1 ^= 1; else d.ph_kv0 ^= 1;
+    if (tile_valid < kTileTok && tid >= tile_valid) {
+      // rows past the chunk end: stale or poisoned V would give 0 * NaN
+      uint8_t* vs = d.smem + kOffV + st * kTileBytes;
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        *reinterpret_cast<uint4*>(vs + (c >> 3) * kHalfBytes + tid * 128 + (c & 7) * 16) =
+            make_uint4(0, 0, 0, 0);
+      fence_proxy_async();
+    }
+    if (group_sync_or(to)) return false;
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t qa = d.sbase + kOffQ, ka = d.sbase + kOffK + st * kTileBytes;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t koff = (k >> 2) * kHalfBytes + (k & 3) * 32;
+        tc_mma(d.tmem, sw128_desc(qa + koff, 16, 1024), sw128_desc(ka + koff, 16, 1024), idesc_s,
+               k > 0);
+      }
+      tc_commit(bar_s(d));
+    }
+    to = !mbar_wait(bar_s(d), d.ph_s);
+    d.ph_s ^= 1;
+    if (j > 0) {
+      to |= !mbar_wait(bar_o(d), d.ph_o);
+      d.ph_o ^= 1;
+    }
+    if (group_sync_or(to)) return false;
+    tc_fence_after();
+    // the other stage is free now (its S and PV products are complete)
+    if (tid == 0 && j + 1 < ntiles) issue_tile(P, d, j + 1, nb, h);
+
+    // row max of the tile
+    float mx = -INFINITY;
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      float v[32];
+      tmem_ld32(trow + q4 * 32, v);
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        if (q4 * 32 + e < tile_valid) mx = fmaxf(mx, v[e] * P.sl2);
+    }
+    const float m_new = (mx > m_run + kRescaleThreshold) ? mx : m_run;
+    const float alpha = ex2(m_run - m_new);
+    if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        float o[32];
+        tmem_ld32(trow + 128 + q4 * 32, o);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] *= alpha;
+        tmem_st32(trow + 128 + q4 * 32, o);
+      }
+    }
+    m_run = m_new;
+    // P = 2^(s - m) as bf16, K-major 128B-swizzled like Q
+    float psum = 0.f;
+    uint8_t* ps = d.smem + kOffP;
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      float v[32];
+      tmem_ld32(trow + q4 * 32, v);
+      uint32_t pk[16];
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) {
+        const float p0 = (q4 * 32 + e < tile_valid) ? ex2(v[e] * P.sl2 - m_run) : 0.f;
+        const float p1 = (q4 * 32 + e + 1 < tile_valid) ? ex2(v[e + 1] * P.sl2 - m_run) : 0.f;
+        psum += p0 + p1;
+        pk[e >> 1] = pack_bf16(p0, p1);
+      }
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        const int jj = (q4 & 1) * 4 + cc;
+        *reinterpret_cast<uint4*>(ps + (q4 >> 1) * kHalfBytes + tid * 128 + ((jj ^ (tid & 7)) << 4)) =
+            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+      }
+    }
+    l_run = l_run * alpha + psum;
+    fence_proxy_async();
+    tc_fence_before();
+    group_sync();
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t pa = d.sbase + kOffP, va = d.sbase + kOffV + st * kTileBytes;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t poff = (k >> 2) * kHalfBytes + (k & 3) * 32;
+        tc_mma(d.tmem + 128, sw128_desc(pa + poff, 16, 1024),
+               sw128_desc(va + k * (16 * 128), kHalfBytes, 1024), idesc_o, (j > 0 || k > 0));
+      }
+      tc_commit(bar_o(d));
+    }
+  }
+  bool to = false;
+  if (ntiles > 0) {
+    to = !mbar_wait(bar_o(d), d.ph_o);
+    d.ph_o ^= 1;
+  }
+  if (group_sync_or(to)) return false;
+  tc_fence_after();
+
+  // epilogue: row tid -> partial slot, then tickets and merges per member
+  const bool valid_row = tid < nrows;
+  int r = -1, hl = 0;
+  ReqInfo ri{};
+  size_t rix = 0;
+  if (valid_row) {
+    r = member_req(P, it, tid / G);
+    hl = tid % G;
+    ri = P.dp.req[r];
+    rix = (((size_t)ri.slot_base + it.slot_j) * P.Hkv + h) * G + hl;
+  }
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) {
+    float o[32];
+    if (ntiles > 0) {
+      tmem_ld32(trow + 128 + q4 * 32, o);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) o[e] = 0.f;
+    }
+    if (valid_row) {
+      float* dst = P.dp.opart + rix * 128 + q4 * 32;
+#pragma unroll
+      for (int e = 0; e < 32; e += 4)
+        __stcg(reinterpret_cast<float4*>(dst + e), make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]));
+    }
+  }
+  if (valid_row) __stcg(&P.dp.mlpart[rix], make_float2(m_run, l_run));
+  __threadfence();
+  __syncwarp();
+  // one ticket per member: its G rows are lanes [lead, lead + G) of this warp
+  const int lead = lane - (lane % G);
+  int last = 0;
+  if (valid_row && hl == 0) {
+    uint32_t* ticket = &P.dp.tickets[(size_t)r * P.Hkv + h];
+    last = atom_add_acq_rel(ticket, 1u) == (uint32_t)ri.n_partials - 1u;
+    if (last) st_relaxed(ticket, 0u);
+  }
+  last = __shfl_sync(0xffffffffu, last, lead);
+  if (valid_row && last) {
+    __threadfence();
+    float M = -INFINITY, L = 0.f;
+    for (int j = 0; j < ri.n_partials; ++j) {
+      const size_t jx = (((size_t)ri.slot_base + j) * P.Hkv + h) * G + hl;
+      const float2 ml = __ldcg(&P.dp.mlpart[jx]);
+      if (ml.x == -INFINITY) continue;
+      const float Mn = fmaxf(M, ml.x);
+      L = L * ex2(M - Mn) + ml.y * ex2(ml.x - Mn);
+      M = Mn;
+    }
+    const bool empty = !(L > 0.f);
+    const float inv = empty ? 0.f : 1.f / L;
+    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(P.out) + ((size_t)r * P.Hq + h * G + hl) * 128;
+    for (int c8 = 0; c8 < 128; c8 += 32) {
+      float acc[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+      for (int j = 0; j < ri.n_partials; ++j) {
+        const size_t jx = (((size_t)ri.slot_base + j) * P.Hkv + h) * G + hl;
+        const float2 ml = __ldcg(&P.dp.mlpart[jx]);
+        if (ml.x == -INFINITY) continue;
+        const float w = ex2(ml.x - M) * inv;
+        const float* src = P.dp.opart + jx * 128 + c8;
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 x = __ldcg(reinterpret_cast<const float4*>(src + e));
+          acc[e] += w * x.x; acc[e + 1] += w * x.y; acc[e + 2] += w * x.z; acc[e + 3] += w * x.w;
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 32; e += 8) store_out<__nv_bfloat16>(dst + c8 + e, acc + e, 8);
+    }
+    if (empty) raise(P, kErrEmpty);
+    if (P.lse) P.lse[(size_t)r * P.Hq + h * G + hl] = empty ? -INFINITY : (M + __log2f(L)) * kLn2;
+  }
+  // the next item overwrites Q, P and TMEM only after every thread is past here
+  tc_fence_before();
+  group_sync();
+  return true;
+}
+
+// Dense items of this CTA, run by warps 0-3.
+__device__ void dense_loop(const Params& P, uint8_t* smem_raw) {
+  const int tid = threadIdx.x, warp = tid >> 5;
+  DenseState d;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
+  d.smem = smem_raw + pad;
+  d.sbase = raw + pad;
+  d.ph_kv0 = d.ph_kv1 = d.ph_s = d.ph_o = 0;
+  volatile int* s_idx = reinterpret_cast<volatile int*>(d.smem + kOffMisc);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(d.smem + kOffMisc + 8);
+  if (tid == 0) {
+    mbar_init(bar_kv(d, 0), 1);
+    mbar_init(bar_kv(d, 1), 1);
+    mbar_init(bar_s(d), 1);
+    mbar_init(bar_o(d), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(s_tmem)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  group_sync();
+  tc_fence_after();
+  d.tmem = *reinterpret_cast<volatile uint32_t*>(s_tmem);
+  for (;;) {
+    if (tid == 0) *s_idx = (int)atomicAdd(&P.dp.ctr[kCtrDense], 1u);
+    group_sync();
+    const int idx = *s_idx;
+    group_sync();
+    if (idx >= P.dp.n_ditems) break;
+    const int4* ip = reinterpret_cast<const int4*>(P.dp.ditems + idx);
+    const int4 a = __ldg(ip), b = __ldg(ip + 1);
+    const Item it{a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    if (!dense_item(P, d, it)) {
+      // a wait gave up: wait (bounded) for this CTA's tensor-core work to drain
+      // before the TMEM is released
+      if (tid == 0) {
+        raise(P, kErrTimeout);
+        tc_commit(bar_s(d));
+        mbar_wait(bar_s(d), d.ph_s);
+      }
+      break;
+    }
+  }
+  tc_fence_before();
+  group_sync();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(d.tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
 // ------------------------------------------------------------ the launch
 
 template <int PATH>
@@ -598,8 +1177,12 @@ __device__ __forceinline__ void run_item(const Params& P, const Item& it, int la
 }
 
 template <int PATH>
-__global__ void __launch_bounds__(kThreads, 1) psattn_fused_decode(const Params P) {
+__global__ void __launch_bounds__(kThreads, 1) psattn_fused_decode(const __grid_constant__ Params P) {
   const int lane = threadIdx.x & 31;
+  if constexpr (PATH == kPathMmaBf16D128) {
+    extern __shared__ uint8_t dyn_smem[];
+    if (P.dp.n_ditems > 0 && threadIdx.x < 128) dense_loop(P, dyn_smem);
+  }
   for (;;) {
     int idx = 0;
     if (lane == 0) idx = (int)atomicAdd(&P.dp.ctr[kCtrWarp], 1u);
@@ -623,8 +1206,49 @@ __global__ void __launch_bounds__(kThreads, 1) psattn_fused_decode(const Params 
 
 template <int PATH>
 cudaError_t launch(const Params& P, int grid, cudaStream_t st) {
-  psattn_fused_decode<PATH><<<grid, kThreads, 0, st>>>(P);
+  const uint32_t smem = (PATH == kPathMmaBf16D128 && P.dp.n_ditems > 0) ? kDenseSmemBytes : 0;
+  if (smem) {
+    static bool attr_set = false;  // once per process; the attribute is per function
+    if (!attr_set) {
+      cudaError_t e = cudaFuncSetAttribute(psattn_fused_decode<PATH>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      attr_set = true;
+    }
+  }
+  psattn_fused_decode<PATH><<<grid, kThreads, smem, st>>>(P);
   return cudaGetLastError();
+}
+
+// Tensor map of the pool for the dense tiles: a 2-D bf16 tensor of
+// [num_blocks * 2 * Hkv * 16 rows][d = 128 columns], boxes of 16 rows x 64
+// columns with the 128-byte swizzle the tcgen05 descriptors expect.
+int encode_kv_map(CUtensorMap* map, const void* pool, int nblocks, int hkv) {
+  using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static EncodeFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !p) {
+      cudaGetLastError();
+      return PSATTN_ERR_CUDA;
+    }
+    fn = reinterpret_cast<EncodeFn>(p);
+  }
+  const cuuint64_t dims[2] = {128, (cuuint64_t)nblocks * 2 * hkv * kBlockSize};
+  const cuuint64_t strides[1] = {128 * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)kBlockSize};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PSATTN_OK : PSATTN_ERR_CUDA;
 }
 
 }  // namespace
@@ -650,6 +1274,11 @@ int psattn_launch_decode(const HostPlan& hp, const DevPlan& dp, const void* q, c
   P.maxb = hp.shape.max_blocks_per_req;
   P.nblocks = hp.shape.num_pool_blocks;
   P.sl2 = hp.shape.scale * kLog2e;
+  std::memset(&P.kv_map, 0, sizeof(P.kv_map));
+  if (hp.path == kPathMmaBf16D128 && dp.n_ditems > 0) {
+    const int rc = encode_kv_map(&P.kv_map, kv_pool, P.nblocks, P.Hkv);
+    if (rc) return rc;
+  }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   switch (hp.path) {

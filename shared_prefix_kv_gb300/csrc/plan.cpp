@@ -29,10 +29,10 @@ namespace {
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
-// Dense prefix tiles are built once the tensor-core item kernel exists; until
-// then every group runs on the per-warp path.
-constexpr bool kDenseBuilt = false;
+// Groups with at least this many q rows (members x G) run as tensor-core tiles.
 constexpr int kDenseMinRows = 32;
+constexpr int kDenseTileTok = 128;    // tokens per tensor-core K/V tile
+constexpr int kDenseMaxChunk = 8192;  // tokens per dense item (its block ids live in smem)
 
 struct Inputs {
   const psattn_shape* s;
@@ -175,8 +175,10 @@ int build(const Inputs& in, int32_t num_sms, HostPlan& hp) {
   for (int g = 0; g < NG; ++g) {
     if (mem[g].empty() || level_len(g) == 0) continue;
     const int64_t rows = (int64_t)mem[g].size() * G;
-    dense[g] = kDenseBuilt && !no_dedup && !(in.flags & PSATTN_NO_TENSOR_PREFIX) &&
-               path == kPathMmaBf16D128 && rows >= kDenseMinRows;
+    // the TMA row coordinate of a block is an int32: (block * 2 + kv) * Hkv * 16
+    const bool tma_ok = (int64_t)s.num_pool_blocks * 2 * Hkv * B <= INT32_MAX;
+    dense[g] = !no_dedup && !(in.flags & PSATTN_NO_TENSOR_PREFIX) &&
+               path == kPathMmaBf16D128 && rows >= kDenseMinRows && tma_ok;
     if (dense[g]) w_dense += ceil_div(mem[g].size(), mpt) * level_len(g);
     else w_warp += ceil_div(mem[g].size(), mpi) * level_len(g);
   }
@@ -186,12 +188,13 @@ int build(const Inputs& in, int32_t num_sms, HostPlan& hp) {
   // warp work; dense items about three per SM.
   const int64_t warps = (int64_t)num_sms * kWarpsPerCta;
   const int64_t c_warp = std::max<int64_t>(64, round_up(ceil_div(w_warp * Hkv, warps * 2), B));
-  const int64_t c_dense =
-      std::max<int64_t>(256, round_up(ceil_div(w_dense * Hkv, (int64_t)num_sms * 3), 64));
-  auto chunking = [&](int64_t len, int64_t target, int32_t* chunk, int32_t* n) {
+  const int64_t c_dense = std::min<int64_t>(
+      kDenseMaxChunk,
+      std::max<int64_t>(256, round_up(ceil_div(w_dense * Hkv, (int64_t)num_sms * 3), kDenseTileTok)));
+  auto chunking = [&](int64_t len, int64_t target, int32_t* chunk, int32_t* n, int64_t unit) {
     if (len <= 0) { *chunk = (int32_t)B; *n = 0; return; }
     int64_t k = ceil_div(len, target);
-    int64_t c = round_up(ceil_div(len, k), B);
+    int64_t c = std::min(round_up(ceil_div(len, k), unit), round_up(target, unit));
     *chunk = (int32_t)c;
     *n = (int32_t)ceil_div(len, c);
   };
@@ -207,7 +210,8 @@ int build(const Inputs& in, int32_t num_sms, HostPlan& hp) {
     gi.dense = dense[g];
     gi.slot_j0 = -1;
     if (mem[g].empty()) { gi.chunk_tok = B; gi.n_chunks = 0; continue; }
-    chunking(level_len(g), dense[g] ? c_dense : c_warp, &gi.chunk_tok, &gi.n_chunks);
+    chunking(level_len(g), dense[g] ? c_dense : c_warp, &gi.chunk_tok, &gi.n_chunks,
+             dense[g] ? kDenseTileTok : B);
     hp.members.insert(hp.members.end(), mem[g].begin(), mem[g].end());
     hp.prefix_chunk_max = std::max(hp.prefix_chunk_max, gi.n_chunks ? gi.chunk_tok : 0);
   }
@@ -226,7 +230,7 @@ int build(const Inputs& in, int32_t num_sms, HostPlan& hp) {
       col += ceil_div(level_len(g), B);
     }
     ri.suffix_col = (int32_t)col;
-    chunking(in.slen[r], c_warp, &ri.suffix_chunk, &ri.suffix_nchunks);
+    chunking(in.slen[r], c_warp, &ri.suffix_chunk, &ri.suffix_nchunks, B);
     hp.suffix_chunk_max = std::max(hp.suffix_chunk_max, ri.suffix_nchunks ? ri.suffix_chunk : 0);
     j += ri.suffix_nchunks;
     ri.slot_base = (int32_t)slot;

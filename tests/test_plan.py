@@ -106,19 +106,28 @@ def test_coverage_exact(name, flags):
 
 @pytest.mark.parametrize("name", ["llama8b", "two_level", "skewed"])
 def test_prefix_read_once_per_group(name):
+    """Each prefix token of a group is read once per (group, KV head) by every
+    item that serves a set of its members: 128/G members per tensor-core tile,
+    8/G per warp item, 1 with de-duplication off."""
     p = W.make(name, small=True)
-    for flags, per_item in [(0, 8 // (p.num_q_heads // p.num_kv_heads)), (ps.NO_DEDUP, 1)]:
+    G = p.num_q_heads // p.num_kv_heads
+    for flags in (0, ps.NO_TENSOR_PREFIX, ps.NO_DEDUP):
         with host_plan(p, flags) as pl:
             t = tables(pl)
             reads = defaultdict(int)
-            for it in t["w"]:
-                if it[0] == 1:
+            for it in np.concatenate([t["w"], t["d"]]):
+                if it[0] in (1, 2):
                     lo, hi = item_span(t, it, p)
                     reads[(int(it[2]), int(it[1]))] += hi - lo
             for g in range(p.num_groups):
-                nmem = int(t["grp"][g][5])
+                nmem, dense = int(t["grp"][g][5]), int(t["grp"][g][7])
                 if nmem == 0:
                     continue
+                per_item = 1 if flags == ps.NO_DEDUP else (128 // G if dense else 8 // G)
+                if flags:
+                    assert not dense
+                else:
+                    assert dense == (nmem * G >= 32)
                 want = int(p.prefix_len[g]) * -(-nmem // per_item)
                 for h in range(p.num_kv_heads):
                     assert reads[(g, h)] == want
