@@ -355,7 +355,7 @@ def make(name: str, seed: Optional[int] = None, *, small: bool = False, poison: 
         if small:
             st = struct_two_level(rng, l1=256, l2=96, n_l2=3, members=12, suffix=(1, 80))
         else:
-            st = struct_two_level(rng)
+            st = struct_two_level(rng, n_l2=override.get("n_groups", 64))
         p = materialize("two_level", st, dtype=BF16, Hq=32, Hkv=8, d=128, **kw)
         return flatten_problem(p) if name == "two_level_flat" else p
     raise KeyError(name)
