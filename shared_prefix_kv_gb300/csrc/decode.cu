@@ -646,23 +646,29 @@ __device__ __forceinline__ void simt_item(const Params& P, const Item& it, int l
 // A dense item is (group, KV head, chunk of the group's level, up to 128/G
 // members): 128 rows of q (member x q head of the KV head; padding rows are
 // zero) against the chunk's K/V, read once for all rows (the prefix partial as
-// a matrix product, BatchLLM section 2.2).  Warps 0-3 of the CTA run it: thread
-// 0 issues the TMA copies and the tcgen05 MMAs, and all 128 threads do the
-// softmax and the epilogue, thread t owning row t (= TMEM lane t).
+// a matrix product, BatchLLM section 2.2).  Five warps of the CTA run it:
 //
-// Per 128-token tile j (stage j & 1 of a double-buffered K/V ring):
-//   TMA: 8 paged blocks x {K, V} x 2 halves of d, 128B-swizzled boxes of
-//        16 rows x 64 columns straight from the pool (tensor map over the pool
-//        as [rows = block*2*Hkv*16][d]);
-//   S = Q K^T   tcgen05.mma kind::f16, M 128, N 128, K 128 (8 steps), fp32 in
-//               TMEM columns [0, 128); Q and K are K-major;
-//   softmax     tcgen05.ld of S, running max m in log2 units, raised only when
-//               the tile max exceeds it by more than 8 (then O is rescaled in
-//               TMEM), P = 2^(s - m) as bf16 into a 128B-swizzled K-major tile;
-//   O += P V    tcgen05.mma, N 128 (d), K 128 tokens, V as the MN-major B
-//               operand, fp32 in TMEM columns [128, 256).
-// Every wait is bounded; a timeout raises the error word and ends the dense
-// work of the CTA without touching the rest.
+//   warps 0-3   softmax and epilogue, thread t owning row t (= TMEM lane t);
+//   warp 4      lane 0 is the control thread: it issues every TMA copy and
+//               every tcgen05 MMA and commit; the other lanes wait.
+//
+// For each 128-token tile g (counted across items, so the rings continue):
+//   TMA       K(g), V(g): 8 paged blocks x 2 halves of d, 128B-swizzled boxes
+//             of 16 rows x 64 columns from the pool (tensor map over the pool
+//             as [rows = block*2*Hkv*16][d]); K and V rings of two stages,
+//             each tile loaded two tiles ahead of its use;
+//   S(g)      = Q K(g)^T, tcgen05.mma kind::f16 M 128 N 128 K 128, fp32 into
+//             TMEM buffer g & 1 (columns 0-127 or 128-255);
+//   softmax   reads S(g) from TMEM, keeps a running max m in log2 units that
+//             moves only when the tile max exceeds it by more than 8 (then O
+//             is rescaled in TMEM), writes P = 2^(s - m) as bf16 into a
+//             128B-swizzled K-major tile;
+//   PV(g)     O += P V(g), V as the MN-major B operand, fp32 in TMEM columns
+//             256-383.
+// The control thread issues S(g + 1) while the softmax works on S(g), so the
+// tensor core and the softmax overlap.  Every wait is bounded: on a timeout
+// the CTA raises the error word, sets an abort flag that makes every later
+// wait return at once, and leaves its dense work.
 
 constexpr int kTileTok = 128;
 constexpr uint32_t kTileBytes = 128 * 128 * 2;          // one 128 x 128 bf16 operand tile
@@ -670,15 +676,26 @@ constexpr uint32_t kHalfBytes = kTileBytes / 2;         // one 64-column half (K
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kTileBytes;                  // 2 stages
 constexpr uint32_t kOffV = 3 * kTileBytes;              // 2 stages
-constexpr uint32_t kOffP = 5 * kTileBytes;
-constexpr uint32_t kOffIds = 6 * kTileBytes;            // block ids of the chunk
+constexpr uint32_t kOffP = 5 * kTileBytes;              // 2 buffers
+constexpr uint32_t kOffEml = 7 * kTileBytes;            // epilogue (m, l) of the 128 rows
 constexpr int kMaxDenseBlocks = 512;                    // chunk <= 8192 tokens
-constexpr uint32_t kOffBar = kOffIds + kMaxDenseBlocks * 4;
-constexpr uint32_t kOffMisc = kOffBar + 64;
-constexpr uint32_t kDenseSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
-constexpr uint32_t kTmemCols = 256;
-constexpr float kRescaleThreshold = 8.0f;               // log2 units
+constexpr uint32_t kOffBar = kOffEml + 128 * 8;         // 13 mbarriers
+constexpr uint32_t kOffMisc = kOffBar + 128;
+constexpr uint32_t kDenseSmemBytes = kOffMisc + 64 + 1024;    // + alignment slack
+static_assert(kDenseSmemBytes <= 232448, "dense tile shared memory exceeds 227 KB");
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemO = 256;                        // O accumulator columns
+#ifndef PSATTN_RESCALE_THRESHOLD
+#define PSATTN_RESCALE_THRESHOLD 8.0f
+#endif
+constexpr float kRescaleThreshold = PSATTN_RESCALE_THRESHOLD;  // log2 units
+// the same limit on P = 2^(s - m): P above 2^threshold means the max moved
+__device__ __forceinline__ float rescale_limit() { return exp2f(kRescaleThreshold); }
+#define kRescaleLimit rescale_limit()
 constexpr uint64_t kWaitLimitNs = 2000000000ull;        // 2 s per wait
+constexpr int kDenseThreads = 224;                      // warps 0-6
+constexpr int kEpiStride = 132;                         // fp32 row stride of the epilogue staging
+
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -710,34 +727,36 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait for phase `parity` of an mbarrier; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Bounded wait for phase `parity` of an mbarrier; false on timeout or when
+// another thread of the dense group has already given up (*abort != 0).
+// Parity waits are sound only when the waiter knows the previous phase has
+// completed and the next one cannot complete before it looks: every wait in
+// this file is placed so that both hold (a stage, buffer or product two phases
+// ahead always depends on something the waiter itself has not yet released).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitLimitNs) return false;
+    if (*abort) return false;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      return false;
+    }
   }
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// named barrier 1 over the 128 threads of warps 0-3
-__device__ __forceinline__ void group_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
-// barrier that also ORs a flag over the 128 threads (uniform abort decisions)
-__device__ __forceinline__ bool group_sync_or(bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n bar.red.or.pred po, 1, 128, pi;\n"
-      " selp.u32 %0, 1, 0, po;\n}\n"
-      : "=r"(r)
-      : "r"((uint32_t)v)
-      : "memory");
-  return r != 0;
-}
+// named barrier 1 over the 224 threads of warps 0-6 (the dense group)
+// (non-aligned form: lanes of the MMA and producer warps may arrive apart)
+__device__ __forceinline__ void dense_sync() { asm volatile("barrier.sync 1, 224;" ::: "memory"); }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
                                             uint32_t bar) {
@@ -828,300 +847,442 @@ __host__ __device__ constexpr uint32_t idesc_bf16_m128_n128(bool b_mn_major) {
          | ((128u >> 4) << 24); // M / 16
 }
 
+
 struct DenseState {
-  uint8_t* smem;      // 1024-aligned
-  uint32_t sbase;     // its shared-space address
-  uint32_t tmem;      // TMEM base (lane 0, column of S)
-  uint32_t ph_kv0, ph_kv1, ph_s, ph_o;
+  uint8_t* smem;       // 1024-aligned
+  uint32_t sbase;      // its shared-space address
+  uint32_t tmem;       // TMEM base address
+  uint32_t g;          // tiles this CTA has run so far (drives every ring phase)
+  volatile int* abort;
 };
 
-__device__ __forceinline__ uint32_t bar_kv(const DenseState& d, int st) {
-  return d.sbase + kOffBar + 8u * st;
-}
-__device__ __forceinline__ uint32_t bar_s(const DenseState& d) { return d.sbase + kOffBar + 16; }
-__device__ __forceinline__ uint32_t bar_o(const DenseState& d) { return d.sbase + kOffBar + 24; }
+// mbarrier slots
+__device__ __forceinline__ uint32_t bar_k(const DenseState& d, uint32_t st) { return d.sbase + kOffBar + 8u * st; }
+__device__ __forceinline__ uint32_t bar_v(const DenseState& d, uint32_t st) { return d.sbase + kOffBar + 16u + 8u * st; }
+__device__ __forceinline__ uint32_t bar_s(const DenseState& d, uint32_t b) { return d.sbase + kOffBar + 32u + 8u * b; }
+__device__ __forceinline__ uint32_t bar_sfree(const DenseState& d, uint32_t b) { return d.sbase + kOffBar + 48u + 8u * b; }
+// one P-ready barrier per P buffer: a softmax warp that runs a tile ahead of
+// the others arrives on the other buffer's barrier and cannot complete a phase
+// for a tile the slower warps have not finished
+__device__ __forceinline__ uint32_t bar_p(const DenseState& d, uint32_t b) { return d.sbase + kOffBar + (b ? 96u : 64u); }
+__device__ __forceinline__ uint32_t bar_pv(const DenseState& d) { return d.sbase + kOffBar + 72u; }
+__device__ __forceinline__ uint32_t bar_vfree(const DenseState& d, uint32_t st) { return d.sbase + kOffBar + 80u + 8u * st; }
 
-// TMA of tile j of the chunk into stage j & 1 (thread 0 only).
-__device__ __forceinline__ void issue_tile(const Params& P, const DenseState& d, int j, int nb,
-                                           int h) {
-  const int st = j & 1;
-  const int* ids = reinterpret_cast<const int*>(d.smem + kOffIds);
-  const int b0 = j * (kTileTok / kBlockSize), b1 = min(nb, b0 + kTileTok / kBlockSize);
-  uint32_t bytes = 0;
-  for (int b = b0; b < b1; ++b)
-    if (ids[b] >= 0) bytes += 4u * kBlockSize * 64u * 2u;  // K and V x two 16 x 64 halves
-  const uint32_t bar = bar_kv(d, st);
-  mbar_expect_tx(bar, bytes);
-  const uint32_t ks = d.sbase + kOffK + st * kTileBytes, vs = d.sbase + kOffV + st * kTileBytes;
-  for (int b = b0; b < b1; ++b) {
-    const int id = ids[b];
-    if (id < 0) continue;
-    const int rk = ((id * 2 + 0) * P.Hkv + h) * kBlockSize;
-    const int rv = ((id * 2 + 1) * P.Hkv + h) * kBlockSize;
-    const uint32_t off = (uint32_t)(b - b0) * (kBlockSize * 128u);
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      tma_load_2d(ks + half * kHalfBytes + off, &P.kv_map, half * 64, rk, bar);
-      tma_load_2d(vs + half * kHalfBytes + off, &P.kv_map, half * 64, rv, bar);
-    }
-  }
-}
-
-// One dense item.  Returns false when a wait timed out (uniform over the group).
-__device__ bool dense_item(const Params& P, DenseState& d, const Item& it) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int G = P.G, h = it.kvh;
-  const Span s = resolve(P, it);
-  const int nrows = s.nmem * G;
-  int ntok = s.t1 - s.t0;
-  if (ntok > kMaxDenseBlocks * kBlockSize) {  // device lengths beyond what was planned
-    if (tid == 0) raise(P, kErrColumn);
-    ntok = kMaxDenseBlocks * kBlockSize;
-  }
-  const int nb = (ntok + kBlockSize - 1) / kBlockSize;
-  const int ntiles = (ntok + kTileTok - 1) / kTileTok;
-
-  // block ids of the chunk -> shared memory (bad ids raise the error word, read -1)
-  int* ids = reinterpret_cast<int*>(d.smem + kOffIds);
-  for (int b = tid; b < nb; b += 128) {
-    int id = -1;
+// TMA of the K (kv = 0) or V (kv = 1) tile of local tile j into stage st, by
+// the 32 lanes of a producer warp: lanes 0-15 each look up one of the tile's 8
+// blocks in the block table (bad ids raise the error word and are skipped) and
+// copy one 16 x 64 half of it; lane 0 first posts the byte count.
+__device__ __forceinline__ void issue_kv(const Params& P, const DenseState& d, const Span& s, int h,
+                                         int kv, uint32_t st, int j, int nb, int lane) {
+  const int b = j * (kTileTok / kBlockSize) + (lane >> 1);
+  int row = -1;
+  if (lane < 16 && b < nb) {
     const int col = s.col0 + b;
     if (col >= P.maxb) {
       raise(P, kErrColumn);
     } else {
-      id = __ldg(&P.bt[(size_t)s.rep * P.maxb + col]);
-      if (id < 0 || id >= P.nblocks) {
-        raise(P, kErrBlockOob);
-        id = -1;
-      }
-    }
-    ids[b] = id;
-  }
-  // Q tile, K-major, 128B swizzle: 16-byte chunk c of row t at
-  // atom (c / 8), row t, position (c % 8) ^ (t % 8)
-  {
-    uint8_t* qs = d.smem + kOffQ;
-    const __nv_bfloat16* qp = nullptr;
-    if (tid < nrows) {
-      const int r = member_req(P, it, tid / G);
-      qp = reinterpret_cast<const __nv_bfloat16*>(P.q) + ((size_t)r * P.Hq + h * G + tid % G) * 128;
-    }
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const uint4 w = qp ? __ldg(reinterpret_cast<const uint4*>(qp + 8 * c)) : make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(qs + (c >> 3) * kHalfBytes + tid * 128 + (((c & 7) ^ (tid & 7)) << 4)) = w;
+      const int id = __ldg(&P.bt[(size_t)s.rep * P.maxb + col]);
+      if (id < 0 || id >= P.nblocks) raise(P, kErrBlockOob);
+      else row = ((id * 2 + kv) * P.Hkv + h) * kBlockSize;
     }
   }
-  fence_proxy_async();
-  group_sync();
-  if (tid == 0 && ntiles > 0) issue_tile(P, d, 0, nb, h);
+  const uint32_t valid = __ballot_sync(0xffffffffu, row >= 0);
+  const uint32_t bar = kv ? bar_v(d, st) : bar_k(d, st);
+  if (lane == 0) mbar_expect_tx(bar, (uint32_t)__popc(valid) * (kBlockSize * 64u * 2u));
+  __syncwarp();
+  if (row >= 0) {
+    const uint32_t dst = d.sbase + (kv ? kOffV : kOffK) + st * kTileBytes + (lane & 1) * kHalfBytes +
+                         (uint32_t)(lane >> 1) * (kBlockSize * 128u);
+    tma_load_2d(dst, &P.kv_map, (lane & 1) * 64, row, bar);
+  }
+}
 
-  const uint32_t trow = d.tmem + ((uint32_t)(warp * 32) << 16);
+// The MMA warp's part of one item (warp 4; lane 0 waits and issues):
+//   S(g) once K(g) has landed and the softmax is done with S(g - 2);
+//   PV(g - 1) once its P is written; commits: S -> bar_s[b], PV -> bar_pv and
+//   bar_vfree[stage of V].
+__device__ void mma_item(const Params& P, DenseState& d, int ntiles) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t g0 = d.g;
   const uint32_t idesc_s = idesc_bf16_m128_n128(false), idesc_o = idesc_bf16_m128_n128(true);
-  float m_run = -INFINITY, l_run = 0.f;
-  for (int j = 0; j < ntiles; ++j) {
-    const int st = j & 1;
-    const int tile_valid = min(kTileTok, ntok - j * kTileTok);
-    bool to = !mbar_wait(bar_kv(d, st), st ? d.ph_kv1 : d.ph_kv0);
-    if (st) d.ph_kv1 ^= 1; else d.ph_kv0 ^= 1;
-    if (tile_valid < kTileTok && tid >= tile_valid) {
-      // rows past the chunk end: stale or poisoned V would give 0 * NaN
-      uint8_t* vs = d.smem + kOffV + st * kTileBytes;
-#pragma unroll
-      for (int c = 0; c < 16; ++c)
-        *reinterpret_cast<uint4*>(vs + (c >> 3) * kHalfBytes + tid * 128 + (c & 7) * 16) =
-            make_uint4(0, 0, 0, 0);
-      fence_proxy_async();
-    }
-    if (group_sync_or(to)) return false;
-    if (tid == 0) {
+  const uint64_t qdesc = sw128_desc(d.sbase + kOffQ, 16, 1024);
+  const uint64_t pdesc0 = sw128_desc(d.sbase + kOffP, 16, 1024);
+  auto wait0 = [&](uint32_t bar, uint32_t parity) -> bool {
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(bar, parity, d.abort);
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+  };
+  auto pv = [&](uint32_t gp) -> bool {
+    if (!wait0(bar_p(d, gp & 1), (gp >> 1) & 1)) return false;
+    if (!wait0(bar_v(d, gp & 1), (gp >> 1) & 1)) return false;
+    if (lane == 0) {
       tc_fence_after();
-      const uint32_t qa = d.sbase + kOffQ, ka = d.sbase + kOffK + st * kTileBytes;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint32_t koff = (k >> 2) * kHalfBytes + (k & 3) * 32;
-        tc_mma(d.tmem, sw128_desc(qa + koff, 16, 1024), sw128_desc(ka + koff, 16, 1024), idesc_s,
-               k > 0);
-      }
-      tc_commit(bar_s(d));
-    }
-    to = !mbar_wait(bar_s(d), d.ph_s);
-    d.ph_s ^= 1;
-    if (j > 0) {
-      to |= !mbar_wait(bar_o(d), d.ph_o);
-      d.ph_o ^= 1;
-    }
-    if (group_sync_or(to)) return false;
-    tc_fence_after();
-    // the other stage is free now (its S and PV products are complete)
-    if (tid == 0 && j + 1 < ntiles) issue_tile(P, d, j + 1, nb, h);
-
-    // row max of the tile
-    float mx = -INFINITY;
-#pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
-      float v[32];
-      tmem_ld32(trow + q4 * 32, v);
-#pragma unroll
-      for (int e = 0; e < 32; ++e)
-        if (q4 * 32 + e < tile_valid) mx = fmaxf(mx, v[e] * P.sl2);
-    }
-    const float m_new = (mx > m_run + kRescaleThreshold) ? mx : m_run;
-    const float alpha = ex2(m_run - m_new);
-    if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        float o[32];
-        tmem_ld32(trow + 128 + q4 * 32, o);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] *= alpha;
-        tmem_st32(trow + 128 + q4 * 32, o);
-      }
-    }
-    m_run = m_new;
-    // P = 2^(s - m) as bf16, K-major 128B-swizzled like Q
-    float psum = 0.f;
-    uint8_t* ps = d.smem + kOffP;
-#pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
-      float v[32];
-      tmem_ld32(trow + q4 * 32, v);
-      uint32_t pk[16];
-#pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        const float p0 = (q4 * 32 + e < tile_valid) ? ex2(v[e] * P.sl2 - m_run) : 0.f;
-        const float p1 = (q4 * 32 + e + 1 < tile_valid) ? ex2(v[e + 1] * P.sl2 - m_run) : 0.f;
-        psum += p0 + p1;
-        pk[e >> 1] = pack_bf16(p0, p1);
-      }
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        const int jj = (q4 & 1) * 4 + cc;
-        *reinterpret_cast<uint4*>(ps + (q4 >> 1) * kHalfBytes + tid * 128 + ((jj ^ (tid & 7)) << 4)) =
-            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-      }
-    }
-    l_run = l_run * alpha + psum;
-    fence_proxy_async();
-    tc_fence_before();
-    group_sync();
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t pa = d.sbase + kOffP, va = d.sbase + kOffV + st * kTileBytes;
+      const uint64_t vdesc = sw128_desc(d.sbase + kOffV + (gp & 1) * kTileBytes, kHalfBytes, 1024);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const uint32_t poff = (k >> 2) * kHalfBytes + (k & 3) * 32;
-        tc_mma(d.tmem + 128, sw128_desc(pa + poff, 16, 1024),
-               sw128_desc(va + k * (16 * 128), kHalfBytes, 1024), idesc_o, (j > 0 || k > 0));
+        tc_mma(d.tmem + kTmemO, pdesc0 + ((poff + (gp & 1) * kTileBytes) >> 4),
+               vdesc + ((k * 16 * 128) >> 4), idesc_o,
+               (gp != g0 || k > 0));
       }
-      tc_commit(bar_o(d));
+      tc_commit(bar_pv(d));
+      tc_commit(bar_vfree(d, gp & 1));
+    }
+    __syncwarp();
+    return true;
+  };
+  for (int j = 0; j < ntiles; ++j) {
+    const uint32_t g = g0 + j, b = g & 1;
+    if (!wait0(bar_k(d, b), (g >> 1) & 1)) return;
+    if (g >= 2 && !wait0(bar_sfree(d, b), ((g >> 1) - 1) & 1)) return;
+    if (lane == 0) {
+      tc_fence_after();
+      const uint64_t kdesc = sw128_desc(d.sbase + kOffK + b * kTileBytes, 16, 1024);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t koff = ((k >> 2) * kHalfBytes + (k & 3) * 32) >> 4;
+        tc_mma(d.tmem + b * 128, qdesc + koff, kdesc + koff, idesc_s, k > 0);
+      }
+      tc_commit(bar_s(d, b));
+    }
+    __syncwarp();
+    if (j >= 1 && !pv(g - 1)) return;
+  }
+  if (ntiles > 0) pv(g0 + ntiles - 1);
+}
+
+// The producer warps' part of one item: warp 5 issues the K copies, warp 6
+// the V copies.  K(g + 2) goes into stage g & 1 once S(g) is done with it,
+// V(g + 2) once PV(g) is.
+__device__ void producer_item(const Params& P, DenseState& d, const Span& s, int h, int kv, int nb,
+                              int ntiles) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t g0 = d.g;
+  auto wait0 = [&](uint32_t bar, uint32_t parity) -> bool {
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(bar, parity, d.abort);
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+  };
+  for (int j = 0; j < min(2, ntiles); ++j) issue_kv(P, d, s, h, kv, (g0 + j) & 1, j, nb, lane);
+  for (int j = 0; j + 2 < ntiles; ++j) {
+    const uint32_t g = g0 + j, b = g & 1;
+    if (!wait0(kv ? bar_vfree(d, b) : bar_s(d, b), (g >> 1) & 1)) return;
+    issue_kv(P, d, s, h, kv, b, j + 2, nb, lane);
+  }
+}
+
+// The Q tile of one item (threads 0-127).
+__device__ void prepare_item(const Params& P, DenseState& d, const Item& it, int nrows) {
+  const int tid = threadIdx.x, G = P.G, h = it.kvh;
+  // Q tile, K-major, 128B swizzle: 16-byte chunk c of row t at
+  // atom (c / 8), row t, position (c % 8) ^ (t % 8)
+  uint8_t* qs = d.smem + kOffQ;
+  const __nv_bfloat16* qp = nullptr;
+  if (tid < nrows) {
+    const int r = member_req(P, it, tid / G);
+    qp = reinterpret_cast<const __nv_bfloat16*>(P.q) + ((size_t)r * P.Hq + h * G + tid % G) * 128;
+  }
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    const uint4 w = qp ? __ldg(reinterpret_cast<const uint4*>(qp + 8 * c)) : make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(qs + (c >> 3) * kHalfBytes + tid * 128 + (((c & 7) ^ (tid & 7)) << 4)) = w;
+  }
+  fence_proxy_async();
+}
+
+// Row max of S(g) (scaled to log2 units) over the tile's valid columns.
+__device__ __forceinline__ float tile_max(uint32_t sa, float sl2, int tile_valid) {
+  float mxa[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) mxa[i] = -INFINITY;
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) {
+    float v[32];
+    tmem_ld32(sa + q4 * 32, v);
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+      if (q4 * 32 + e < tile_valid) mxa[e & 7] = fmaxf(mxa[e & 7], v[e]);
+  }
+  return fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
+               fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7]))) * sl2;
+}
+
+// One pass over S(g) of this thread's row: P = 2^(s * sl2 - m) as bf16 into
+// the row of the P buffer (K-major, 128B swizzle), columns past tile_valid as
+// 0 (kFull: all 128 columns are valid, no masks).  Returns the row sum of P
+// (fp32); *pmax gets the largest P of the row (bf16 precision), which tells
+// whether the running max m is still within 2^8 of the row's values.
+template <bool kFull>
+__device__ __forceinline__ float softmax_pass(uint32_t sa, float sl2, float m, int tile_valid,
+                                              uint8_t* pbuf, int tid, float* pmax) {
+  const float2 sl2_2 = make_float2(sl2, sl2), negm_2 = make_float2(-m, -m);
+  float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  __nv_bfloat162 mx2 = __floats2bfloat162_rn(0.f, 0.f);
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) {
+    float v[32];
+    tmem_ld32(sa + q4 * 32, v);
+    uint32_t pk[16];
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      const float2 x = __ffma2_rn(make_float2(v[e], v[e + 1]), sl2_2, negm_2);
+      float p0 = ex2(x.x), p1 = ex2(x.y);
+      if (!kFull) {
+        const int c = q4 * 32 + e;
+        p0 = c < tile_valid ? p0 : 0.f;
+        p1 = c + 1 < tile_valid ? p1 : 0.f;
+      }
+      acc[(e >> 1) & 1] = __fadd2_rn(acc[(e >> 1) & 1], make_float2(p0, p1));
+      const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
+      mx2 = __hmax2(mx2, pp);
+      pk[e >> 1] = *reinterpret_cast<const uint32_t*>(&pp);
+    }
+    // tokens 32 q4 .. 32 q4 + 31: atom q4 / 2, 16-byte chunks 4 (q4 % 2) .. + 3
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      const int jj = (q4 & 1) * 4 + cc;
+      *reinterpret_cast<uint4*>(pbuf + (q4 >> 1) * kHalfBytes + tid * 128 + ((jj ^ (tid & 7)) << 4)) =
+          make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
     }
   }
-  bool to = false;
-  if (ntiles > 0) {
-    to = !mbar_wait(bar_o(d), d.ph_o);
-    d.ph_o ^= 1;
-  }
-  if (group_sync_or(to)) return false;
-  tc_fence_after();
+  *pmax = fmaxf(__bfloat162float(mx2.x), __bfloat162float(mx2.y));
+  return (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
+}
 
-  // epilogue: row tid -> partial slot, then tickets and merges per member
-  const bool valid_row = tid < nrows;
-  int r = -1, hl = 0;
-  ReqInfo ri{};
-  size_t rix = 0;
-  if (valid_row) {
-    r = member_req(P, it, tid / G);
-    hl = tid % G;
-    ri = P.dp.req[r];
-    rix = (((size_t)ri.slot_base + it.slot_j) * P.Hkv + h) * G + hl;
-  }
+// The last tile of a chunk may be partial: its (rare) masked pass is kept out
+// of line so that the full-tile pass keeps its registers.
+__device__ __noinline__ float softmax_pass_masked(uint32_t sa, float sl2, float m, int tile_valid,
+                                                  uint8_t* pbuf, int tid, float* pmax) {
+  return softmax_pass<false>(sa, sl2, m, tile_valid, pbuf, tid, pmax);
+}
+
+__device__ __forceinline__ float softmax_pass_any(uint32_t sa, float sl2, float m, int tile_valid,
+                                                  uint8_t* pbuf, int tid, float* pmax) {
+  return tile_valid == kTileTok ? softmax_pass<true>(sa, sl2, m, tile_valid, pbuf, tid, pmax)
+                                : softmax_pass_masked(sa, sl2, m, tile_valid, pbuf, tid, pmax);
+}
+
+// Cold path of the softmax: some row's tile max grew by more than 2^8 over its
+// running max.  Recompute P for the warp (rows that did not grow keep their
+// max), then rescale O and l of the grown rows once PV(g - 1) is complete.
+__device__ __noinline__ bool softmax_regrow(const Params& P, DenseState& d, uint32_t sa,
+                                            uint32_t trow, int tile_valid, uint8_t* pbuf,
+                                            uint32_t g, bool grow, float* m_run, float* l_run,
+                                            float* psum) {
+  const int tid = threadIdx.x;
+  const float m_new = grow ? tile_max(sa, P.sl2, tile_valid) : *m_run;
+  const float alpha = ex2(*m_run - m_new);
+  float pm;
+  *psum = softmax_pass_any(sa, P.sl2, m_new, tile_valid, pbuf, tid, &pm);
+  if (!mbar_wait(bar_pv(d), (g - 1) & 1, d.abort)) return false;
+  tc_fence_after();
 #pragma unroll
   for (int q4 = 0; q4 < 4; ++q4) {
     float o[32];
-    if (ntiles > 0) {
-      tmem_ld32(trow + 128 + q4 * 32, o);
-    } else {
+    tmem_ld32(trow + kTmemO + q4 * 32, o);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) o[e] = 0.f;
-    }
-    if (valid_row) {
-      float* dst = P.dp.opart + rix * 128 + q4 * 32;
-#pragma unroll
-      for (int e = 0; e < 32; e += 4)
-        __stcg(reinterpret_cast<float4*>(dst + e), make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]));
-    }
+    for (int e = 0; e < 32; ++e) o[e] *= alpha;
+    tmem_st32(trow + kTmemO + q4 * 32, o);
   }
-  if (valid_row) __stcg(&P.dp.mlpart[rix], make_float2(m_run, l_run));
+  *l_run *= alpha;
+  *m_run = m_new;
+  return true;
+}
+
+// Merge of the rows of the members (bits of lastmask, member index within this
+// warp) whose last partial the calling warp just wrote: one row per lane, d in
+// chunks of 16 with the loads of all partials in flight together.
+__device__ __noinline__ void dense_merge_rows(const Params& P, const Item& it, int h, int nrows,
+                                              uint32_t lastmask) {
+  const int G = P.G, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   __threadfence();
-  __syncwarp();
-  // one ticket per member: its G rows are lanes [lead, lead + G) of this warp
-  const int lead = lane - (lane % G);
-  int last = 0;
-  if (valid_row && hl == 0) {
-    uint32_t* ticket = &P.dp.tickets[(size_t)r * P.Hkv + h];
-    last = atom_add_acq_rel(ticket, 1u) == (uint32_t)ri.n_partials - 1u;
-    if (last) st_relaxed(ticket, 0u);
-  }
-  last = __shfl_sync(0xffffffffu, last, lead);
-  if (valid_row && last) {
-    __threadfence();
-    float M = -INFINITY, L = 0.f;
-    for (int j = 0; j < ri.n_partials; ++j) {
-      const size_t jx = (((size_t)ri.slot_base + j) * P.Hkv + h) * G + hl;
-      const float2 ml = __ldcg(&P.dp.mlpart[jx]);
-      if (ml.x == -INFINITY) continue;
-      const float Mn = fmaxf(M, ml.x);
-      L = L * ex2(M - Mn) + ml.y * ex2(ml.x - Mn);
-      M = Mn;
+  const int row = warp * 32 + lane;
+  if (((lastmask >> (lane / G)) & 1) && row < nrows) {
+    const int r = member_req(P, it, row / G), hl = row % G;
+    const ReqInfo ri = P.dp.req[r];
+    const size_t base = (((size_t)ri.slot_base) * P.Hkv + h) * G + hl;
+    const size_t jstride = (size_t)P.Hkv * G;
+    float M = -INFINITY;
+#pragma unroll 4
+    for (int jp = 0; jp < ri.n_partials; ++jp)
+      M = fmaxf(M, __ldcg(&P.dp.mlpart[base + jp * jstride]).x);
+    float L = 0.f;
+#pragma unroll 4
+    for (int jp = 0; jp < ri.n_partials; ++jp) {
+      const float2 ml = __ldcg(&P.dp.mlpart[base + jp * jstride]);
+      L += (ml.x == -INFINITY) ? 0.f : ml.y * ex2(ml.x - M);
     }
     const bool empty = !(L > 0.f);
     const float inv = empty ? 0.f : 1.f / L;
-    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(P.out) + ((size_t)r * P.Hq + h * G + hl) * 128;
-    for (int c8 = 0; c8 < 128; c8 += 32) {
-      float acc[32];
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(P.out) + ((size_t)r * P.Hq + h * G + hl) * 128;
+    for (int c = 0; c < 128; c += 16) {
+      float acc[16];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-      for (int j = 0; j < ri.n_partials; ++j) {
-        const size_t jx = (((size_t)ri.slot_base + j) * P.Hkv + h) * G + hl;
-        const float2 ml = __ldcg(&P.dp.mlpart[jx]);
-        if (ml.x == -INFINITY) continue;
-        const float w = ex2(ml.x - M) * inv;
-        const float* src = P.dp.opart + jx * 128 + c8;
+      for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+#pragma unroll 2
+      for (int jp = 0; jp < ri.n_partials; ++jp) {
+        const float2 ml = __ldcg(&P.dp.mlpart[base + jp * jstride]);
+        const float w = (ml.x == -INFINITY) ? 0.f : ex2(ml.x - M) * inv;
+        const float* src = P.dp.opart + (base + jp * jstride) * 128 + c;
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
+        for (int e = 0; e < 16; e += 4) {
           const float4 x = __ldcg(reinterpret_cast<const float4*>(src + e));
           acc[e] += w * x.x; acc[e + 1] += w * x.y; acc[e + 2] += w * x.z; acc[e + 3] += w * x.w;
         }
       }
-#pragma unroll
-      for (int e = 0; e < 32; e += 8) store_out<__nv_bfloat16>(dst + c8 + e, acc + e, 8);
+      store_out<__nv_bfloat16>(out + c, acc, 8);
+      store_out<__nv_bfloat16>(out + c + 8, acc + 8, 8);
     }
     if (empty) raise(P, kErrEmpty);
     if (P.lse) P.lse[(size_t)r * P.Hq + h * G + hl] = empty ? -INFINITY : (M + __log2f(L)) * kLn2;
   }
-  // the next item overwrites Q, P and TMEM only after every thread is past here
-  tc_fence_before();
-  group_sync();
-  return true;
 }
 
-// Dense items of this CTA, run by warps 0-3.
+// The softmax warps' part of one item, then the epilogue (partial slot,
+// tickets, merges).  Returns early (abort set) on a timeout.
+__device__ void softmax_item(const Params& P, DenseState& d, const Item& it, const Span& s,
+                             int ntok, int ntiles, int nrows) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = P.G, h = it.kvh;
+  const uint32_t g0 = d.g;
+  const uint32_t trow = d.tmem + ((uint32_t)(warp * 32) << 16);
+  float m_run = -INFINITY, l_run = 0.f;
+  for (int j = 0; j < ntiles; ++j) {
+    const uint32_t g = g0 + j, b = g & 1;
+    const int tile_valid = min(kTileTok, ntok - j * kTileTok);
+    uint8_t* pbuf = d.smem + kOffP + b * kTileBytes;
+    if (!mbar_wait(bar_s(d, b), (g >> 1) & 1, d.abort)) return;
+    // P buffer b was last read by PV(g - 2)
+    if (j >= 2 && !mbar_wait(bar_vfree(d, b), ((g >> 1) - 1) & 1, d.abort)) return;
+    tc_fence_after();
+    const uint32_t sa = trow + b * 128;
+    // P against the running max (the tile's own max on the first tile of the
+    // item, when O is still empty); rows whose values outgrew the running max
+    // by more than 2^8 (P > 256) are redone with their new max (rare)
+    if (j == 0) m_run = tile_max(sa, P.sl2, tile_valid);
+    float pmax;
+    float psum = softmax_pass_any(sa, P.sl2, m_run, tile_valid, pbuf, tid, &pmax);
+    const bool grow = pmax > kRescaleLimit;
+    if (j > 0 && __any_sync(0xffffffffu, grow)) {
+      if (!softmax_regrow(P, d, sa, trow, tile_valid, pbuf, g, grow, &m_run, &l_run, &psum))
+        return;
+    }
+    l_run = (j == 0) ? psum : l_run + psum;
+    // S(g) has been read: the MMA warp may reuse this TMEM buffer
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_sfree(d, b));
+    if (tile_valid < kTileTok) {
+      // rows past the chunk end may hold anything (even NaN): zero them in V
+      // before PV reads them (0 * NaN would poison O)
+      if (!mbar_wait(bar_v(d, b), (g >> 1) & 1, d.abort)) return;
+      if (tid >= tile_valid) {
+        uint8_t* vs = d.smem + kOffV + b * kTileBytes;
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          *reinterpret_cast<uint4*>(vs + (c >> 3) * kHalfBytes + tid * 128 + (c & 7) * 16) =
+              make_uint4(0, 0, 0, 0);
+      }
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_p(d, b));
+  }
+  // O is final once PV(last) is done.  A parity wait for phase k is only sound
+  // once phase k - 1 has completed (else it would read the pending phase k - 1
+  // as the completed phase k of the same parity); this warp has only seen
+  // PV(last - 2) complete so far, so PV(last - 1) is waited for first.
+  if (ntiles > 1 && !mbar_wait(bar_pv(d), (g0 + ntiles - 2) & 1, d.abort)) return;
+  if (ntiles > 0) {
+    if (!mbar_wait(bar_pv(d), (g0 + ntiles - 1) & 1, d.abort)) return;
+    tc_fence_after();
+  }
+
+  // ---- epilogue.  O rows go through shared memory (the K/V stages are free
+  // now) so that each member's G rows leave as contiguous 512-byte rows and the
+  // merges read them back coalesced, lanes across d.
+  float* E = reinterpret_cast<float*>(d.smem + kOffK);     // [128][kEpiStride] fp32
+  float2* Eml = reinterpret_cast<float2*>(d.smem + kOffEml);  // [128] (m, l)
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) {
+    float o[32];
+    if (ntiles > 0) {
+      tmem_ld32(trow + kTmemO + q4 * 32, o);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) o[e] = 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < 32; e += 4)
+      *reinterpret_cast<float4*>(E + tid * kEpiStride + q4 * 32 + e) =
+          make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+  }
+  Eml[tid] = make_float2(m_run, l_run);
+  tc_fence_before();
+  __syncwarp();
+  // this warp's rows: 32 / G members of G rows each
+  const int mpw = 32 / G;
+  for (int mu = 0; mu < mpw; ++mu) {
+    const int row0 = warp * 32 + mu * G;
+    if (row0 >= nrows) break;
+    const int r = member_req(P, it, row0 / G);
+    const ReqInfo ri = P.dp.req[r];
+    float* dst = P.dp.opart + ((((size_t)ri.slot_base + it.slot_j) * P.Hkv + h) * G) * 128;
+    for (int x = lane; x < G * 32; x += 32) {  // G rows x 32 float4
+      const int rr = x >> 5, c = (x & 31) * 4;
+      __stcg(reinterpret_cast<float4*>(dst + rr * 128 + c),
+             *reinterpret_cast<const float4*>(E + (row0 + rr) * kEpiStride + c));
+    }
+    if (lane < G)
+      __stcg(&P.dp.mlpart[(((size_t)ri.slot_base + it.slot_j) * P.Hkv + h) * G + lane],
+             Eml[row0 + lane]);
+  }
+  __threadfence();
+  __syncwarp();
+  // tickets: lane mu takes the ticket of member mu of this warp
+  int last = 0;
+  int r_mine = -1;
+  if (lane < mpw && warp * 32 + lane * G < nrows) {
+    r_mine = member_req(P, it, (warp * 32 + lane * G) / G);
+    const ReqInfo ri = P.dp.req[r_mine];
+    uint32_t* ticket = &P.dp.tickets[(size_t)r_mine * P.Hkv + h];
+    last = atom_add_acq_rel(ticket, 1u) == (uint32_t)ri.n_partials - 1u;
+    if (last) st_relaxed(ticket, 0u);
+  }
+  uint32_t lastmask = __ballot_sync(0xffffffffu, last);
+  // merge the rows of every member whose last partial this was
+  if (lastmask) dense_merge_rows(P, it, h, nrows, lastmask);
+  // the staging buffer aliases the K/V stages the next item's TMA writes
+  fence_proxy_async();
+}
+
+// Dense items of this CTA, run by warps 0-6 (224 threads).
 __device__ void dense_loop(const Params& P, uint8_t* smem_raw) {
   const int tid = threadIdx.x, warp = tid >> 5;
+  const bool control = (tid == 128);
   DenseState d;
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
   d.smem = smem_raw + pad;
   d.sbase = raw + pad;
-  d.ph_kv0 = d.ph_kv1 = d.ph_s = d.ph_o = 0;
+  d.g = 0;
   volatile int* s_idx = reinterpret_cast<volatile int*>(d.smem + kOffMisc);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(d.smem + kOffMisc + 8);
-  if (tid == 0) {
-    mbar_init(bar_kv(d, 0), 1);
-    mbar_init(bar_kv(d, 1), 1);
-    mbar_init(bar_s(d), 1);
-    mbar_init(bar_o(d), 1);
+  d.abort = reinterpret_cast<volatile int*>(d.smem + kOffMisc + 16);
+  if (control) {
+    *d.abort = 0;
+    for (uint32_t st = 0; st < 2; ++st) {
+      mbar_init(bar_k(d, st), 1);
+      mbar_init(bar_v(d, st), 1);
+      mbar_init(bar_s(d, st), 1);
+      mbar_init(bar_sfree(d, st), 4);
+    }
+    mbar_init(bar_p(d, 0), 4);
+    mbar_init(bar_p(d, 1), 4);
+    mbar_init(bar_pv(d), 1);
+    mbar_init(bar_vfree(d, 0), 1);
+    mbar_init(bar_vfree(d, 1), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) {
@@ -1132,31 +1293,46 @@ __device__ void dense_loop(const Params& P, uint8_t* smem_raw) {
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
-  group_sync();
+  dense_sync();
   tc_fence_after();
   d.tmem = *reinterpret_cast<volatile uint32_t*>(s_tmem);
   for (;;) {
-    if (tid == 0) *s_idx = (int)atomicAdd(&P.dp.ctr[kCtrDense], 1u);
-    group_sync();
+    if (control) *s_idx = (int)atomicAdd(&P.dp.ctr[kCtrDense], 1u);
+    dense_sync();
     const int idx = *s_idx;
-    group_sync();
-    if (idx >= P.dp.n_ditems) break;
+    const bool stop = idx >= P.dp.n_ditems || *d.abort;
+    dense_sync();
+    if (stop) break;
     const int4* ip = reinterpret_cast<const int4*>(P.dp.ditems + idx);
     const int4 a = __ldg(ip), b = __ldg(ip + 1);
     const Item it{a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    if (!dense_item(P, d, it)) {
-      // a wait gave up: wait (bounded) for this CTA's tensor-core work to drain
-      // before the TMEM is released
-      if (tid == 0) {
-        raise(P, kErrTimeout);
-        tc_commit(bar_s(d));
-        mbar_wait(bar_s(d), d.ph_s);
-      }
-      break;
+    const Span s = resolve(P, it);
+    const int nrows = s.nmem * P.G;
+    int ntok = s.t1 - s.t0;
+    if (ntok > kMaxDenseBlocks * kBlockSize) {  // device lengths beyond what was planned
+      if (control) raise(P, kErrColumn);
+      ntok = kMaxDenseBlocks * kBlockSize;
+    }
+    const int nb = (ntok + kBlockSize - 1) / kBlockSize;
+    const int ntiles = (ntok + kTileTok - 1) / kTileTok;
+    if (tid < 128) prepare_item(P, d, it, nrows);
+    dense_sync();
+    if (tid < 128) softmax_item(P, d, it, s, ntok, ntiles, nrows);
+    else if (warp == 4) mma_item(P, d, ntiles);
+    else if (warp == 5 || warp == 6) producer_item(P, d, s, it.kvh, warp - 5, nb, ntiles);
+    tc_fence_before();
+    dense_sync();
+    d.g += ntiles;
+  }
+  if (*d.abort && control) {
+    raise(P, kErrTimeout);
+    // give tensor-core work already issued time to drain before the TMEM is released
+    const uint64_t t0 = global_ns();
+    while (global_ns() - t0 < 10000000ull) {
     }
   }
   tc_fence_before();
-  group_sync();
+  dense_sync();
   if (warp == 0) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(d.tmem),
@@ -1181,7 +1357,7 @@ __global__ void __launch_bounds__(kThreads, 1) psattn_fused_decode(const __grid_
   const int lane = threadIdx.x & 31;
   if constexpr (PATH == kPathMmaBf16D128) {
     extern __shared__ uint8_t dyn_smem[];
-    if (P.dp.n_ditems > 0 && threadIdx.x < 128) dense_loop(P, dyn_smem);
+    if (P.dp.n_ditems > 0 && threadIdx.x < kDenseThreads) dense_loop(P, dyn_smem);
   }
   for (;;) {
     int idx = 0;

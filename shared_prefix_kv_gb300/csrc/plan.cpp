@@ -32,7 +32,7 @@ inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 // Groups with at least this many q rows (members x G) run as tensor-core tiles.
 constexpr int kDenseMinRows = 32;
 constexpr int kDenseTileTok = 128;    // tokens per tensor-core K/V tile
-constexpr int kDenseMaxChunk = 8192;  // tokens per dense item (its block ids live in smem)
+constexpr int kDenseMaxChunk = 8192;  // tokens per dense item
 
 struct Inputs {
   const psattn_shape* s;
