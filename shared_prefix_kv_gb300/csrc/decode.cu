@@ -1070,7 +1070,9 @@ __device__ __noinline__ bool softmax_regrow(const Params& P, DenseState& d, uint
                                             uint32_t g, bool grow, float* m_run, float* l_run,
                                             float* psum) {
   const int tid = threadIdx.x;
-  const float m_new = grow ? tile_max(sa, P.sl2, tile_valid) : *m_run;
+  // tcgen05.ld is warp-collective: every lane reads the tile max, then selects
+  const float tmax = tile_max(sa, P.sl2, tile_valid);
+  const float m_new = grow ? tmax : *m_run;
   const float alpha = ex2(*m_run - m_new);
   float pm;
   *psum = softmax_pass_any(sa, P.sl2, m_new, tile_valid, pbuf, tid, &pm);
