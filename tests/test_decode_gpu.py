@@ -119,6 +119,28 @@ def test_edge_simt_shapes(dtype, d):
     _check(p, *_run(p))
 
 
+def test_dense_running_max_regrow():
+    """A dense prefix tile whose later K/V tiles score far above the first:
+    the tensor-core softmax must move its running max mid-chunk (recompute P
+    and rescale O in TMEM), for some rows and not others."""
+    _lib()
+    p = _custom(32, 8, 128, W.BF16, groups=[1000], parent=None,
+                members=[0] * 12 + [-1], suffix=[3, 40, 0, 77, 5, 16, 9, 1, 130, 2, 2, 2, 50])
+    rng = np.random.default_rng(5)
+    cols = -(-1000 // 16)
+    blocks = p.block_table[0, :cols]
+    vals = W.bf16_bits_to_f32(p.pool[blocks])            # [cols][2][Hkv][16][d]
+    scale = np.ones((cols, 1, 1, 1, 1), np.float32)
+    scale[cols // 3:] = 4.0                               # K of the later tokens x4
+    scale[2 * cols // 3:] = rng.uniform(0.5, 6.0, size=(cols - 2 * cols // 3, 1, 1, 1, 1))
+    vals[:, 0:1] *= scale
+    # the scaled scores make attention peaky (|out| ~ |v|): V is scaled down so
+    # that the bf16 rounding of the output stays well inside the 1e-2 bound
+    vals[:, 1:2] *= 0.25
+    p.pool[blocks] = W.f32_to_bf16_bits(vals)
+    _check(p, *_run(p))
+
+
 def test_edge_three_level_chain():
     _lib()
     p = _custom(32, 8, 128, W.BF16, groups=[48, 20, 7, 100], parent=[-1, 0, 1, 0],
