@@ -83,6 +83,12 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
   return old;
 }
 
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void st_relaxed(uint32_t* p, uint32_t v) {
   asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -646,55 +652,65 @@ __device__ __forceinline__ void simt_item(const Params& P, const Item& it, int l
 // A dense item is (group, KV head, chunk of the group's level, up to 128/G
 // members): 128 rows of q (member x q head of the KV head; padding rows are
 // zero) against the chunk's K/V, read once for all rows (the prefix partial as
-// a matrix product, BatchLLM section 2.2).  Five warps of the CTA run it:
+// a matrix product, BatchLLM section 2.2).  Seven warps of the CTA run it:
 //
 //   warps 0-3   softmax and epilogue, thread t owning row t (= TMEM lane t);
-//   warp 4      lane 0 is the control thread: it issues every TMA copy and
-//               every tcgen05 MMA and commit; the other lanes wait.
+//   warp 4      lane 0 issues every tcgen05 MMA and commit;
+//   warps 5, 6  TMA producers of the K and the V tiles.
 //
 // For each 128-token tile g (counted across items, so the rings continue):
 //   TMA       K(g), V(g): 8 paged blocks x 2 halves of d, 128B-swizzled boxes
 //             of 16 rows x 64 columns from the pool (tensor map over the pool
-//             as [rows = block*2*Hkv*16][d]); K and V rings of two stages,
-//             each tile loaded two tiles ahead of its use;
+//             as [rows = block*2*Hkv*16][d]), into K and V rings of three
+//             stages; a stage is refilled as soon as the MMA that read it is
+//             done;
 //   S(g)      = Q K(g)^T, tcgen05.mma kind::f16 M 128 N 128 K 128, fp32 into
 //             TMEM buffer g & 1 (columns 0-127 or 128-255);
 //   softmax   reads S(g) from TMEM, keeps a running max m in log2 units that
 //             moves only when the tile max exceeds it by more than 8 (then O
-//             is rescaled in TMEM), writes P = 2^(s - m) as bf16 into a
-//             128B-swizzled K-major tile;
-//   PV(g)     O += P V(g), V as the MN-major B operand, fp32 in TMEM columns
+//             is rescaled in TMEM), writes P = 2^(s - m) as bf16 pairs back
+//             into TMEM (columns 384-447 or 448-511, one row per lane);
+//   PV(g)     O += P V(g), P as the A operand straight from TMEM, V as the
+//             MN-major B operand from shared memory, fp32 in TMEM columns
 //             256-383.
-// The control thread issues S(g + 1) while the softmax works on S(g), so the
-// tensor core and the softmax overlap.  Every wait is bounded: on a timeout
-// the CTA raises the error word, sets an abort flag that makes every later
-// wait return at once, and leaves its dense work.
+// The MMA warp issues S(g + 1) while the softmax works on S(g), so the tensor
+// core and the softmax overlap.  Every wait is bounded: on a timeout the CTA
+// raises the error word, sets an abort flag that makes every later wait
+// return at once, and leaves its dense work.
 
 constexpr int kTileTok = 128;
 constexpr uint32_t kTileBytes = 128 * 128 * 2;          // one 128 x 128 bf16 operand tile
 constexpr uint32_t kHalfBytes = kTileBytes / 2;         // one 64-column half (K atom)
+constexpr int kStages = 3;                              // K and V ring depth
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kTileBytes;                  // 2 stages
-constexpr uint32_t kOffV = 3 * kTileBytes;              // 2 stages
-constexpr uint32_t kOffP = 5 * kTileBytes;              // 2 buffers
-constexpr uint32_t kOffEml = 7 * kTileBytes;            // epilogue (m, l) of the 128 rows
+constexpr uint32_t kOffK = kTileBytes;                  // kStages K stages
+constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;  // kStages V stages
+// Between items the stages are idle: the epilogue stages O ([128][128] fp32)
+// over the first two K stages and the merge buffers (4 warps x 32 KB) over the
+// rest.
+constexpr uint32_t kOffE = kOffK;
+constexpr uint32_t kOffMergeBuf = kOffK + 2 * kTileBytes;
+constexpr uint32_t kOffEml = kOffV + kStages * kTileBytes;  // epilogue (m, l) of the 128 rows
+static_assert(kOffMergeBuf + 4 * 32768 <= kOffEml, "merge buffers overrun the stages");
 constexpr int kMaxDenseBlocks = 512;                    // chunk <= 8192 tokens
-constexpr uint32_t kOffBar = kOffEml + 128 * 8;         // 13 mbarriers
-constexpr uint32_t kOffMisc = kOffBar + 128;
-constexpr uint32_t kDenseSmemBytes = kOffMisc + 64 + 1024;    // + alignment slack
+constexpr uint32_t kOffBar = kOffEml + 128 * 8;         // 20 mbarriers
+constexpr uint32_t kOffMisc = kOffBar + 160;
+constexpr uint32_t kOffMergeBar = kOffMisc + 64;        // 2 mbarriers per softmax warp
+constexpr uint32_t kDenseSmemBytes = kOffMergeBar + 64 + 1024;  // + alignment slack
 static_assert(kDenseSmemBytes <= 232448, "dense tile shared memory exceeds 227 KB");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 256;                        // O accumulator columns
-#ifndef PSATTN_RESCALE_THRESHOLD
-#define PSATTN_RESCALE_THRESHOLD 8.0f
+constexpr uint32_t kTmemP = 384;                        // two P buffers of 64 columns
+// A row's running max m moves only when the row's sum of P = 2^(s - m) over
+// a tile exceeds 2^PSATTN_RESCALE_LOG2_SUM (then some P exceeds 2^8: m is at
+// least 8 below the row's values).  P, O and l stay far inside the bf16 and
+// fp32 ranges below that, so only this bound on their size matters.
+#ifndef PSATTN_RESCALE_LOG2_SUM
+#define PSATTN_RESCALE_LOG2_SUM 15
 #endif
-constexpr float kRescaleThreshold = PSATTN_RESCALE_THRESHOLD;  // log2 units
-// the same limit on P = 2^(s - m): P above 2^threshold means the max moved
-__device__ __forceinline__ float rescale_limit() { return exp2f(kRescaleThreshold); }
-#define kRescaleLimit rescale_limit()
+constexpr float kRescaleSumLimit = (float)(1u << PSATTN_RESCALE_LOG2_SUM);
 constexpr uint64_t kWaitLimitNs = 2000000000ull;        // 2 s per wait
 constexpr int kDenseThreads = 224;                      // warps 0-6
-constexpr int kEpiStride = 132;                         // fp32 row stride of the epilogue staging
 
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -750,6 +766,15 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// bulk copy global -> shared (16-byte aligned, size a multiple of 16),
+// completion counted in bytes on an mbarrier
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -785,6 +810,48 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, 
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// The same with the A operand read from TMEM (rows in lanes 0-127, K along
+// columns, two bf16 per 32-bit column).
+__device__ __forceinline__ void tc_mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane; the caller waits
+// (tmem_wait_st) before the values are published
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 32 consecutive 32-bit columns of this thread's TMEM lane, without the wait
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
 // 32 consecutive fp32 columns of this thread's TMEM lane
@@ -856,24 +923,35 @@ struct DenseState {
   volatile int* abort;
 };
 
-// mbarrier slots
+// mbarrier slots.  Tile g uses K/V stage g % kStages (completion number
+// g / kStages on that stage's barriers) and TMEM S and P buffers g % 2
+// (completion number g / 2).
+//   k[st], v[st]      K / V of the stage landed (TMA byte count)
+//   kfree[st]         S of the stage's tile done (its K may be overwritten)
+//   vfree[st]         PV of the stage's tile done (its V may be overwritten)
+//   s[b]              S(g) in TMEM buffer b
+//   sfree[b]          the four softmax warps have read S buffer b
+//   p[b]              the four softmax warps have written P buffer b (one
+//                     barrier per buffer: a warp a tile ahead arrives on the
+//                     other one and cannot complete a phase for a tile the
+//                     slower warps have not finished)
+//   pfree[b]          PV of P buffer b done (P may be rewritten; O updated)
 __device__ __forceinline__ uint32_t bar_k(const DenseState& d, uint32_t st) { return d.sbase + kOffBar + 8u * st; }
-__device__ __forceinline__ uint32_t bar_v(const DenseState& d, uint32_t st) { return d.sbase + kOffBar + 16u + 8u * st; }
-__device__ __forceinline__ uint32_t bar_s(const DenseState& d, uint32_t b) { return d.sbase + kOffBar + 32u + 8u * b; }
-__device__ __forceinline__ uint32_t bar_sfree(const DenseState& d, uint32_t b) { return d.sbase + kOffBar + 48u + 8u * b; }
-// one P-ready barrier per P buffer: a softmax warp that runs a tile ahead of
-// the others arrives on the other buffer's barrier and cannot complete a phase
-// for a tile the slower warps have not finished
-__device__ __forceinline__ uint32_t bar_p(const DenseState& d, uint32_t b) { return d.sbase + kOffBar + (b ? 96u : 64u); }
-__device__ __forceinline__ uint32_t bar_pv(const DenseState& d) { return d.sbase + kOffBar + 72u; }
-__device__ __forceinline__ uint32_t bar_vfree(const DenseState& d, uint32_t st) { return d.sbase + kOffBar + 80u + 8u * st; }
+__device__ __forceinline__ uint32_t bar_v(const DenseState& d, uint32_t st) { return d.sbase + kOffBar + 24u + 8u * st; }
+__device__ __forceinline__ uint32_t bar_s(const DenseState& d, uint32_t b) { return d.sbase + kOffBar + 48u + 8u * b; }
+__device__ __forceinline__ uint32_t bar_sfree(const DenseState& d, uint32_t b) { return d.sbase + kOffBar + 64u + 8u * b; }
+__device__ __forceinline__ uint32_t bar_p(const DenseState& d, uint32_t b) { return d.sbase + kOffBar + 80u + 8u * b; }
+__device__ __forceinline__ uint32_t bar_pfree(const DenseState& d, uint32_t b) { return d.sbase + kOffBar + 96u + 8u * b; }
+__device__ __forceinline__ uint32_t bar_kfree(const DenseState& d, uint32_t st) { return d.sbase + kOffBar + 112u + 8u * st; }
+__device__ __forceinline__ uint32_t bar_vfree(const DenseState& d, uint32_t st) { return d.sbase + kOffBar + 136u + 8u * st; }
 
-// TMA of the K (kv = 0) or V (kv = 1) tile of local tile j into stage st, by
-// the 32 lanes of a producer warp: lanes 0-15 each look up one of the tile's 8
-// blocks in the block table (bad ids raise the error word and are skipped) and
-// copy one 16 x 64 half of it; lane 0 first posts the byte count.
-__device__ __forceinline__ void issue_kv(const Params& P, const DenseState& d, const Span& s, int h,
-                                         int kv, uint32_t st, int j, int nb, int lane) {
+// Block-table lookup for the K or V tile of local tile j, by the 32 lanes of a
+// producer warp: lanes 0-15 each take one of the tile's 8 blocks (lane / 2)
+// and one 64-column half of it (lane % 2); returns the pool row of that block
+// half's 16 tokens, -1 for lanes without one (bad ids raise the error word
+// and are skipped).
+__device__ __forceinline__ int kv_row(const Params& P, const Span& s, int h, int kv, int j, int nb,
+                                      int lane) {
   const int b = j * (kTileTok / kBlockSize) + (lane >> 1);
   int row = -1;
   if (lane < 16 && b < nb) {
@@ -886,6 +964,13 @@ __device__ __forceinline__ void issue_kv(const Params& P, const DenseState& d, c
       else row = ((id * 2 + kv) * P.Hkv + h) * kBlockSize;
     }
   }
+  return row;
+}
+
+// TMA of one K or V tile into stage st from the rows kv_row looked up; lane 0
+// first posts the byte count.
+__device__ __forceinline__ void issue_kv(const Params& P, const DenseState& d, int kv, uint32_t st,
+                                         int row, int lane) {
   const uint32_t valid = __ballot_sync(0xffffffffu, row >= 0);
   const uint32_t bar = kv ? bar_v(d, st) : bar_k(d, st);
   if (lane == 0) mbar_expect_tx(bar, (uint32_t)__popc(valid) * (kBlockSize * 64u * 2u));
@@ -898,52 +983,51 @@ __device__ __forceinline__ void issue_kv(const Params& P, const DenseState& d, c
 }
 
 // The MMA warp's part of one item (warp 4; lane 0 waits and issues):
-//   S(g) once K(g) has landed and the softmax is done with S(g - 2);
-//   PV(g - 1) once its P is written; commits: S -> bar_s[b], PV -> bar_pv and
-//   bar_vfree[stage of V].
+//   S(g) once K(g) has landed and the softmax is done with S(g - 2); commits
+//   to s[g % 2] and kfree[stage];
+//   PV(g - 1) once its P is written and its V has landed; commits to
+//   pfree[(g - 1) % 2] and vfree[stage].
 __device__ void mma_item(const Params& P, DenseState& d, int ntiles) {
   const int lane = threadIdx.x & 31;
   const uint32_t g0 = d.g;
   const uint32_t idesc_s = idesc_bf16_m128_n128(false), idesc_o = idesc_bf16_m128_n128(true);
   const uint64_t qdesc = sw128_desc(d.sbase + kOffQ, 16, 1024);
-  const uint64_t pdesc0 = sw128_desc(d.sbase + kOffP, 16, 1024);
   auto wait0 = [&](uint32_t bar, uint32_t parity) -> bool {
     int ok = 1;
     if (lane == 0) ok = mbar_wait(bar, parity, d.abort);
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
   };
   auto pv = [&](uint32_t gp) -> bool {
+    const uint32_t st = gp % kStages;
     if (!wait0(bar_p(d, gp & 1), (gp >> 1) & 1)) return false;
-    if (!wait0(bar_v(d, gp & 1), (gp >> 1) & 1)) return false;
+    if (!wait0(bar_v(d, st), (gp / kStages) & 1)) return false;
     if (lane == 0) {
       tc_fence_after();
-      const uint64_t vdesc = sw128_desc(d.sbase + kOffV + (gp & 1) * kTileBytes, kHalfBytes, 1024);
+      const uint64_t vdesc = sw128_desc(d.sbase + kOffV + st * kTileBytes, kHalfBytes, 1024);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint32_t poff = (k >> 2) * kHalfBytes + (k & 3) * 32;
-        tc_mma(d.tmem + kTmemO, pdesc0 + ((poff + (gp & 1) * kTileBytes) >> 4),
-               vdesc + ((k * 16 * 128) >> 4), idesc_o,
-               (gp != g0 || k > 0));
-      }
-      tc_commit(bar_pv(d));
-      tc_commit(bar_vfree(d, gp & 1));
+      for (int k = 0; k < 8; ++k)  // 16 tokens of P = 8 TMEM columns per step
+        tc_mma_ta(d.tmem + kTmemO, d.tmem + kTmemP + (gp & 1) * 64 + k * 8,
+                  vdesc + ((k * 16 * 128) >> 4), idesc_o, (gp != g0 || k > 0));
+      tc_commit(bar_pfree(d, gp & 1));
+      tc_commit(bar_vfree(d, st));
     }
     __syncwarp();
     return true;
   };
   for (int j = 0; j < ntiles; ++j) {
-    const uint32_t g = g0 + j, b = g & 1;
-    if (!wait0(bar_k(d, b), (g >> 1) & 1)) return;
+    const uint32_t g = g0 + j, b = g & 1, st = g % kStages;
+    if (!wait0(bar_k(d, st), (g / kStages) & 1)) return;
     if (g >= 2 && !wait0(bar_sfree(d, b), ((g >> 1) - 1) & 1)) return;
     if (lane == 0) {
       tc_fence_after();
-      const uint64_t kdesc = sw128_desc(d.sbase + kOffK + b * kTileBytes, 16, 1024);
+      const uint64_t kdesc = sw128_desc(d.sbase + kOffK + st * kTileBytes, 16, 1024);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const uint32_t koff = ((k >> 2) * kHalfBytes + (k & 3) * 32) >> 4;
         tc_mma(d.tmem + b * 128, qdesc + koff, kdesc + koff, idesc_s, k > 0);
       }
       tc_commit(bar_s(d, b));
+      tc_commit(bar_kfree(d, st));
     }
     __syncwarp();
     if (j >= 1 && !pv(g - 1)) return;
@@ -952,8 +1036,11 @@ __device__ void mma_item(const Params& P, DenseState& d, int ntiles) {
 }
 
 // The producer warps' part of one item: warp 5 issues the K copies, warp 6
-// the V copies.  K(g + 2) goes into stage g & 1 once S(g) is done with it,
-// V(g + 2) once PV(g) is.
+// the V copies.  The first kStages tiles go straight into their stages (the
+// previous item is done with every stage); tile g >= kStages waits for the
+// stage's previous tile g - kStages to be consumed (kfree / vfree).  The block
+// ids of a tile are looked up before that wait, so the lookup's latency
+// overlaps it.
 __device__ void producer_item(const Params& P, DenseState& d, const Span& s, int h, int kv, int nb,
                               int ntiles) {
   const int lane = threadIdx.x & 31;
@@ -963,23 +1050,27 @@ __device__ void producer_item(const Params& P, DenseState& d, const Span& s, int
     if (lane == 0) ok = mbar_wait(bar, parity, d.abort);
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
   };
-  for (int j = 0; j < min(2, ntiles); ++j) issue_kv(P, d, s, h, kv, (g0 + j) & 1, j, nb, lane);
-  for (int j = 0; j + 2 < ntiles; ++j) {
-    const uint32_t g = g0 + j, b = g & 1;
-    if (!wait0(kv ? bar_vfree(d, b) : bar_s(d, b), (g >> 1) & 1)) return;
-    issue_kv(P, d, s, h, kv, b, j + 2, nb, lane);
+  for (int j = 0; j < ntiles; ++j) {
+    const uint32_t g = g0 + j, st = g % kStages;
+    const int row = kv_row(P, s, h, kv, j, nb, lane);
+    if (j >= kStages &&
+        !wait0(kv ? bar_vfree(d, st) : bar_kfree(d, st), ((g / kStages) - 1) & 1))
+      return;
+    issue_kv(P, d, kv, st, row, lane);
   }
 }
 
-// The Q tile of one item (threads 0-127).
-__device__ void prepare_item(const Params& P, DenseState& d, const Item& it, int nrows) {
+// The Q tile of one item (threads 0-127); returns the request of the
+// thread's row (-1 past the item's rows).
+__device__ int prepare_item(const Params& P, DenseState& d, const Item& it, int nrows) {
   const int tid = threadIdx.x, G = P.G, h = it.kvh;
   // Q tile, K-major, 128B swizzle: 16-byte chunk c of row t at
   // atom (c / 8), row t, position (c % 8) ^ (t % 8)
   uint8_t* qs = d.smem + kOffQ;
   const __nv_bfloat16* qp = nullptr;
+  int r = -1;
   if (tid < nrows) {
-    const int r = member_req(P, it, tid / G);
+    r = member_req(P, it, tid / G);
     qp = reinterpret_cast<const __nv_bfloat16*>(P.q) + ((size_t)r * P.Hq + h * G + tid % G) * 128;
   }
 #pragma unroll
@@ -988,6 +1079,7 @@ __device__ void prepare_item(const Params& P, DenseState& d, const Item& it, int
     *reinterpret_cast<uint4*>(qs + (c >> 3) * kHalfBytes + tid * 128 + (((c & 7) ^ (tid & 7)) << 4)) = w;
   }
   fence_proxy_async();
+  return r;
 }
 
 // Row max of S(g) (scaled to log2 units) over the tile's valid columns.
@@ -1007,25 +1099,28 @@ __device__ __forceinline__ float tile_max(uint32_t sa, float sl2, int tile_valid
                fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7]))) * sl2;
 }
 
-// One pass over S(g) of this thread's row: P = 2^(s * sl2 - m) as bf16 into
-// the row of the P buffer (K-major, 128B swizzle), columns past tile_valid as
-// 0 (kFull: all 128 columns are valid, no masks).  Returns the row sum of P
-// (fp32); *pmax gets the largest P of the row (bf16 precision), which tells
-// whether the running max m is still within 2^8 of the row's values.
+// One pass over S(g) of this thread's row: P = 2^(s * sl2 - m) as bf16 pairs
+// into the row's TMEM lane at pa (token 2c and 2c + 1 in column c, the lower
+// token in the low half), columns past tile_valid as 0 (kFull: all 128
+// columns are valid, no masks).  Returns the row sum of P (fp32).  The next
+// 32 columns of S are loaded while this 32 are computed.
 template <bool kFull>
 __device__ __forceinline__ float softmax_pass(uint32_t sa, float sl2, float m, int tile_valid,
-                                              uint8_t* pbuf, int tid, float* pmax) {
+                                              uint32_t pa) {
   const float2 sl2_2 = make_float2(sl2, sl2), negm_2 = make_float2(-m, -m);
   float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-  __nv_bfloat162 mx2 = __floats2bfloat162_rn(0.f, 0.f);
+  uint32_t r[2][32];
+  tmem_ld32_async(sa, r[0]);
+  tmem_wait_ld();
 #pragma unroll
   for (int q4 = 0; q4 < 4; ++q4) {
-    float v[32];
-    tmem_ld32(sa + q4 * 32, v);
+    if (q4 + 1 < 4) tmem_ld32_async(sa + (q4 + 1) * 32, r[(q4 + 1) & 1]);
+    const uint32_t* v = r[q4 & 1];
     uint32_t pk[16];
 #pragma unroll
     for (int e = 0; e < 32; e += 2) {
-      const float2 x = __ffma2_rn(make_float2(v[e], v[e + 1]), sl2_2, negm_2);
+      const float2 x = __ffma2_rn(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
+                                  sl2_2, negm_2);
       float p0 = ex2(x.x), p1 = ex2(x.y);
       if (!kFull) {
         const int c = q4 * 32 + e;
@@ -1034,49 +1129,45 @@ __device__ __forceinline__ float softmax_pass(uint32_t sa, float sl2, float m, i
       }
       acc[(e >> 1) & 1] = __fadd2_rn(acc[(e >> 1) & 1], make_float2(p0, p1));
       const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
-      mx2 = __hmax2(mx2, pp);
       pk[e >> 1] = *reinterpret_cast<const uint32_t*>(&pp);
     }
-    // tokens 32 q4 .. 32 q4 + 31: atom q4 / 2, 16-byte chunks 4 (q4 % 2) .. + 3
-#pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
-      const int jj = (q4 & 1) * 4 + cc;
-      *reinterpret_cast<uint4*>(pbuf + (q4 >> 1) * kHalfBytes + tid * 128 + ((jj ^ (tid & 7)) << 4)) =
-          make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-    }
+    tmem_st16(pa + q4 * 16, pk);
+    if (q4 + 1 < 4) tmem_wait_ld();
   }
-  *pmax = fmaxf(__bfloat162float(mx2.x), __bfloat162float(mx2.y));
+  tmem_wait_st();
   return (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
 }
 
-// The last tile of a chunk may be partial: its (rare) masked pass is kept out
-// of line so that the full-tile pass keeps its registers.
+// Both passes are separate functions: scheduled on their own, away from the
+// rest of the kernel, the full pass runs about twice as fast.
+__device__ __noinline__ float softmax_pass_full(uint32_t sa, float sl2, float m, uint32_t pa) {
+  return softmax_pass<true>(sa, sl2, m, kTileTok, pa);
+}
 __device__ __noinline__ float softmax_pass_masked(uint32_t sa, float sl2, float m, int tile_valid,
-                                                  uint8_t* pbuf, int tid, float* pmax) {
-  return softmax_pass<false>(sa, sl2, m, tile_valid, pbuf, tid, pmax);
+                                                  uint32_t pa) {
+  return softmax_pass<false>(sa, sl2, m, tile_valid, pa);
 }
 
 __device__ __forceinline__ float softmax_pass_any(uint32_t sa, float sl2, float m, int tile_valid,
-                                                  uint8_t* pbuf, int tid, float* pmax) {
-  return tile_valid == kTileTok ? softmax_pass<true>(sa, sl2, m, tile_valid, pbuf, tid, pmax)
-                                : softmax_pass_masked(sa, sl2, m, tile_valid, pbuf, tid, pmax);
+                                                  uint32_t pa) {
+  return tile_valid == kTileTok ? softmax_pass_full(sa, sl2, m, pa)
+                                : softmax_pass_masked(sa, sl2, m, tile_valid, pa);
 }
 
-// Cold path of the softmax: some row's tile max grew by more than 2^8 over its
-// running max.  Recompute P for the warp (rows that did not grow keep their
+// Cold path of the softmax: some row's tile sum of P outgrew the limit (its
+// running max is stale).  Recompute P for the warp (rows that did not grow keep their
 // max), then rescale O and l of the grown rows once PV(g - 1) is complete.
 __device__ __noinline__ bool softmax_regrow(const Params& P, DenseState& d, uint32_t sa,
-                                            uint32_t trow, int tile_valid, uint8_t* pbuf,
+                                            uint32_t trow, int tile_valid, uint32_t pa,
                                             uint32_t g, bool grow, float* m_run, float* l_run,
                                             float* psum) {
-  const int tid = threadIdx.x;
   // tcgen05.ld is warp-collective: every lane reads the tile max, then selects
   const float tmax = tile_max(sa, P.sl2, tile_valid);
   const float m_new = grow ? tmax : *m_run;
   const float alpha = ex2(*m_run - m_new);
-  float pm;
-  *psum = softmax_pass_any(sa, P.sl2, m_new, tile_valid, pbuf, tid, &pm);
-  if (!mbar_wait(bar_pv(d), (g - 1) & 1, d.abort)) return false;
+  *psum = softmax_pass_any(sa, P.sl2, m_new, tile_valid, pa);
+  // PV(g - 1) done: pfree of its buffer, completion (g - 1) / 2
+  if (!mbar_wait(bar_pfree(d, (g - 1) & 1), ((g - 1) >> 1) & 1, d.abort)) return false;
   tc_fence_after();
 #pragma unroll
   for (int q4 = 0; q4 < 4; ++q4) {
@@ -1091,82 +1182,217 @@ __device__ __noinline__ bool softmax_regrow(const Params& P, DenseState& d, uint
   return true;
 }
 
-// Merge of the rows of the members (bits of lastmask, member index within this
-// warp) whose last partial the calling warp just wrote: one row per lane, d in
-// chunks of 16 with the loads of all partials in flight together.
-__device__ __noinline__ void dense_merge_rows(const Params& P, const Item& it, int h, int nrows,
-                                              uint32_t lastmask) {
-  const int G = P.G, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __threadfence();
-  const int row = warp * 32 + lane;
-  if (((lastmask >> (lane / G)) & 1) && row < nrows) {
-    const int r = member_req(P, it, row / G), hl = row % G;
-    const ReqInfo ri = P.dp.req[r];
-    const size_t base = (((size_t)ri.slot_base) * P.Hkv + h) * G + hl;
-    const size_t jstride = (size_t)P.Hkv * G;
-    float M = -INFINITY;
-#pragma unroll 4
-    for (int jp = 0; jp < ri.n_partials; ++jp)
-      M = fmaxf(M, __ldcg(&P.dp.mlpart[base + jp * jstride]).x);
-    float L = 0.f;
-#pragma unroll 4
-    for (int jp = 0; jp < ri.n_partials; ++jp) {
-      const float2 ml = __ldcg(&P.dp.mlpart[base + jp * jstride]);
-      L += (ml.x == -INFINITY) ? 0.f : ml.y * ex2(ml.x - M);
+// End of a dense item for the 32 rows of the calling softmax warp (mpw = 32/G
+// members of G rows; O staged in E, (m, l) in Eml).  Lane mu speaks for member
+// mu (request r, partial slots from sb, np of them; peek = its ticket as read
+// before the last PV completed).  If the peek shows every other partial
+// already in, this item is the last one and merges straight from E without
+// writing its own partial; otherwise the member's rows go to its partial slot
+// and its ticket is taken, the last arriver merging.  The merge: lane = row
+// finds (M, 1/L) over the row's partials and writes the LSE; then each other
+// partial's rows come into a per-warp shared-memory buffer by cp.async (two
+// buffers, the next partial in flight while this one is added) and are added
+// into E lanes across d, a float4 per lane; E then leaves as bf16 rows.
+__device__ __noinline__ void dense_finish(const Params& P, const Item& it, DenseState& d, float* E,
+                                          const float2* Eml, int nrows, int r, int sb, int np,
+                                          uint32_t peek) {
+  constexpr uint32_t kAll = 0xffffffffu;
+  const int G = P.G, h = it.kvh, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mpw = 32 / G;
+  const bool valid = lane < mpw && warp * 32 + lane * G < nrows && r >= 0;
+  uint32_t* ticket = valid ? &P.dp.tickets[(size_t)r * P.Hkv + h] : nullptr;
+  const uint32_t need = (uint32_t)np - 1u;
+  const bool fast = valid && peek == need;
+  const uint32_t wmask = __ballot_sync(kAll, valid && !fast);
+  for (uint32_t m = wmask; m; m &= m - 1) {
+    const int mu = __ffs(m) - 1;
+    const int sbm = __shfl_sync(kAll, sb, mu);
+    const int row0 = warp * 32 + mu * G;
+    const size_t rix0 = (((size_t)sbm + it.slot_j) * P.Hkv + h) * G;
+    float* dst = P.dp.opart + rix0 * 128;
+    for (int x = lane; x < G * 32; x += 32) {
+      const int rr = x >> 5, c = x & 31, row = row0 + rr;
+      __stcg(reinterpret_cast<float4*>(dst + rr * 128 + c * 4),
+             *reinterpret_cast<const float4*>(E + row * 128 + ((c ^ (row & 7)) << 2)));
+    }
+    if (lane < G) __stcg(&P.dp.mlpart[rix0 + lane], Eml[row0 + lane]);
+  }
+  bool last = fast;
+  if (wmask) {
+    __threadfence();
+    __syncwarp();
+    if (valid && !fast) last = atom_add_acq_rel(ticket, 1u) == need;
+  }
+  if (last) st_relaxed(ticket, 0u);  // every partial is in: ready for the next launch
+  const uint32_t mmask = __ballot_sync(kAll, last);
+  if (!mmask) return;
+  __threadfence();  // with the ticket read above: the other partials are visible
+
+  // lane = row: (M, 1/L) over the row's partials, every (m, l) load in flight
+  // at once; the weights of the first kNp partials stay in registers
+  constexpr int kNp = 8;
+  const int row = warp * 32 + lane, mu_r = lane / G, hl = lane % G;
+  const int sb_r = __shfl_sync(kAll, sb, mu_r);
+  const int np_r = __shfl_sync(kAll, np, mu_r);
+  const int r_r = __shfl_sync(kAll, r, mu_r);
+  const bool mrow = (mmask >> mu_r) & 1;
+  const size_t rstride = (size_t)P.Hkv * G;  // between slots of one row
+  const size_t rix_r = ((size_t)sb_r * P.Hkv + h) * G + hl;
+  float2 mlv[kNp];
+#pragma unroll
+  for (int j = 0; j < kNp; ++j)
+    mlv[j] = (mrow && j < np_r && j != it.slot_j) ? __ldcg(&P.dp.mlpart[rix_r + j * rstride])
+                                                   : make_float2(-INFINITY, 0.f);
+  float M = -INFINITY, inv = 0.f, wown = 0.f;
+  float wv[kNp];
+  if (mrow) {
+    const float2 own = Eml[row];
+    M = own.x;
+#pragma unroll
+    for (int j = 0; j < kNp; ++j) M = fmaxf(M, mlv[j].x);
+    for (int j = kNp; j < np_r; ++j)
+      if (j != it.slot_j) M = fmaxf(M, __ldcg(&P.dp.mlpart[rix_r + j * rstride]).x);
+    float L = own.x == -INFINITY ? 0.f : own.y * ex2(own.x - M);
+#pragma unroll
+    for (int j = 0; j < kNp; ++j)
+      if (mlv[j].x != -INFINITY) L += mlv[j].y * ex2(mlv[j].x - M);
+    for (int j = kNp; j < np_r; ++j) {
+      if (j == it.slot_j) continue;
+      const float2 ml = __ldcg(&P.dp.mlpart[rix_r + j * rstride]);
+      if (ml.x != -INFINITY) L += ml.y * ex2(ml.x - M);
     }
     const bool empty = !(L > 0.f);
-    const float inv = empty ? 0.f : 1.f / L;
-    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(P.out) + ((size_t)r * P.Hq + h * G + hl) * 128;
-    for (int c = 0; c < 128; c += 16) {
-      float acc[16];
+    inv = empty ? 0.f : 1.f / L;
+    wown = (empty || own.x == -INFINITY) ? 0.f : ex2(own.x - M) * inv;
+    if (empty) raise(P, kErrEmpty);
+    if (P.lse) P.lse[(size_t)r_r * P.Hq + h * G + hl] = empty ? -INFINITY : (M + __log2f(L)) * kLn2;
+  }
 #pragma unroll
-      for (int e = 0; e < 16; ++e) acc[e] = 0.f;
-#pragma unroll 2
-      for (int jp = 0; jp < ri.n_partials; ++jp) {
-        const float2 ml = __ldcg(&P.dp.mlpart[base + jp * jstride]);
-        const float w = (ml.x == -INFINITY) ? 0.f : ex2(ml.x - M) * inv;
-        const float* src = P.dp.opart + (base + jp * jstride) * 128 + c;
-#pragma unroll
-        for (int e = 0; e < 16; e += 4) {
-          const float4 x = __ldcg(reinterpret_cast<const float4*>(src + e));
-          acc[e] += w * x.x; acc[e + 1] += w * x.y; acc[e + 2] += w * x.z; acc[e + 3] += w * x.w;
+  for (int j = 0; j < kNp; ++j) wv[j] = mlv[j].x == -INFINITY ? 0.f : ex2(mlv[j].x - M) * inv;
+
+  const uint32_t rmask = __ballot_sync(kAll, mrow);
+  const int jmax = __reduce_max_sync(kAll, mrow ? np_r : 0);
+  // E row of a merged row, scaled by the row's own weight
+  for (uint32_t m = rmask; m; m &= m - 1) {
+    const int rl = __ffs(m) - 1, rw = warp * 32 + rl;
+    const float w = __shfl_sync(kAll, wown, rl);
+    float4* e = reinterpret_cast<float4*>(E + rw * 128 + ((lane ^ (rw & 7)) << 2));
+    const float4 v = *e;
+    *e = make_float4(v.x * w, v.y * w, v.z * w, v.w * w);
+  }
+  // (rows with no partial but this one: E is already the output)
+  if (jmax > (it.slot_j == 0 ? 1 : 0)) {
+    // The other partials come in by bulk copy, one G-row block (contiguous in
+    // the partial store) per member, into two [32][128] fp32 buffers per warp in
+    // the idle K/V stages, each with its mbarrier.
+    const uint32_t buf0 = d.sbase + kOffMergeBuf + warp * (2u * 32 * 128 * 4);
+    const uint32_t mb0 = d.sbase + kOffMergeBar + warp * 16u;
+    // bit bi: parity of buffer bi's next completion (kept across items)
+    volatile uint32_t* phase_word = reinterpret_cast<volatile uint32_t*>(d.smem + kOffMisc + 32) + warp;
+    uint32_t phase = *phase_word;
+    fence_proxy_async();
+    __syncwarp();
+    auto issue = [&](int j, int bi) {
+      const bool cp = valid && ((mmask >> lane) & 1) && j < np && j != it.slot_j;
+      const uint32_t n = __popc(__ballot_sync(kAll, cp));
+      const uint32_t bar = mb0 + 8u * bi;
+      if (lane == 0) mbar_expect_tx(bar, n * (uint32_t)G * 512u);
+      __syncwarp();
+      if (cp)
+        bulk_g2s(buf0 + (uint32_t)bi * (32u * 128 * 4) + (uint32_t)(lane * G) * 512u,
+                 P.dp.opart + ((((size_t)sb + j) * P.Hkv + h) * G) * 128, (uint32_t)G * 512u, bar);
+    };
+    // E rows += w (this lane's row weight) x buffer bi, once its copies are in
+    auto accumulate = [&](float wl, int bi) -> bool {
+      if (!mbar_wait(mb0 + 8u * bi, (phase >> bi) & 1, d.abort)) return false;
+      phase ^= 1u << bi;
+      const float* bj = reinterpret_cast<const float*>(d.smem + kOffMergeBuf) + warp * (2 * 32 * 128) +
+                        bi * (32 * 128);
+      for (uint32_t m = rmask; m; m &= m - 1) {
+        const int rl = __ffs(m) - 1, rw = warp * 32 + rl;
+        const float w = __shfl_sync(kAll, wl, rl);
+        if (w != 0.f) {  // (an empty partial, or one past the row's count, adds nothing)
+          float4* e = reinterpret_cast<float4*>(E + rw * 128 + ((lane ^ (rw & 7)) << 2));
+          const float4 o = *reinterpret_cast<const float4*>(bj + rl * 128 + lane * 4);
+          float4 v = *e;
+          v.x += w * o.x; v.y += w * o.y; v.z += w * o.z; v.w += w * o.w;
+          *e = v;
         }
       }
-      store_out<__nv_bfloat16>(out + c, acc, 8);
-      store_out<__nv_bfloat16>(out + c + 8, acc + 8, 8);
+      // the buffer is read: the next bulk copy into it may start
+      fence_proxy_async();
+      __syncwarp();
+      return true;
+    };
+    auto next_j = [&](int j) { return (j + 1 == it.slot_j) ? j + 2 : j + 1; };
+    // two-deep pipeline: partial j is added while the next one is in flight
+    int bi = 0;
+    issue(it.slot_j == 0 ? 1 : 0, 0);
+    auto step = [&](int j, float wl) -> bool {
+      const int jn = next_j(j);
+      if (jn < jmax) issue(jn, bi ^ 1);
+      if (!accumulate(wl, bi)) return false;
+      bi ^= 1;
+      return true;
+    };
+#pragma unroll
+    for (int j = 0; j < kNp; ++j)
+      if (j < jmax && j != it.slot_j && !step(j, wv[j])) return;
+    for (int j = kNp; j < jmax; ++j) {  // rows with more partials: weights from (m, l) again
+      if (j == it.slot_j) continue;
+      float wl = 0.f;
+      if (mrow && j < np_r) {
+        const float2 ml = __ldcg(&P.dp.mlpart[rix_r + j * rstride]);
+        wl = ml.x == -INFINITY ? 0.f : ex2(ml.x - M) * inv;
+      }
+      if (!step(j, wl)) return;
     }
-    if (empty) raise(P, kErrEmpty);
-    if (P.lse) P.lse[(size_t)r * P.Hq + h * G + hl] = empty ? -INFINITY : (M + __log2f(L)) * kLn2;
+    if (lane == 0) *phase_word = phase;
+  }
+  // the merged rows leave as bf16
+  for (uint32_t m = rmask; m; m &= m - 1) {
+    const int rl = __ffs(m) - 1, rw = warp * 32 + rl;
+    const int rq = __shfl_sync(kAll, r_r, rl);
+    const float4 v = *reinterpret_cast<const float4*>(E + rw * 128 + ((lane ^ (rw & 7)) << 2));
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(P.out) +
+                         ((size_t)rq * P.Hq + h * G + rl % G) * 128 + lane * 4;
+    *reinterpret_cast<uint2*>(out) = make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
   }
 }
 
-// The softmax warps' part of one item, then the epilogue (partial slot,
-// tickets, merges).  Returns early (abort set) on a timeout.
-__device__ void softmax_item(const Params& P, DenseState& d, const Item& it, const Span& s,
-                             int ntok, int ntiles, int nrows) {
+// The softmax warps' part of one item, then the epilogue.  r_row is the
+// request of this thread's row (-1 past the item's rows).  Returns early
+// (abort set) on a timeout.
+__device__ void softmax_item(const Params& P, DenseState& d, const Item& it, int ntok, int ntiles,
+                             int nrows, int r_row) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int G = P.G, h = it.kvh;
   const uint32_t g0 = d.g;
   const uint32_t trow = d.tmem + ((uint32_t)(warp * 32) << 16);
+  // the row's partial slots, needed only at the end (the load hides behind the tiles)
+  int sb_row = 0, np_row = 0;
+  if (r_row >= 0) {
+    const ReqInfo ri = P.dp.req[r_row];
+    sb_row = ri.slot_base;
+    np_row = ri.n_partials;
+  }
   float m_run = -INFINITY, l_run = 0.f;
   for (int j = 0; j < ntiles; ++j) {
     const uint32_t g = g0 + j, b = g & 1;
     const int tile_valid = min(kTileTok, ntok - j * kTileTok);
-    uint8_t* pbuf = d.smem + kOffP + b * kTileBytes;
+    const uint32_t pa = trow + kTmemP + b * 64;
     if (!mbar_wait(bar_s(d, b), (g >> 1) & 1, d.abort)) return;
     // P buffer b was last read by PV(g - 2)
-    if (j >= 2 && !mbar_wait(bar_vfree(d, b), ((g >> 1) - 1) & 1, d.abort)) return;
+    if (j >= 2 && !mbar_wait(bar_pfree(d, b), ((g >> 1) - 1) & 1, d.abort)) return;
     tc_fence_after();
     const uint32_t sa = trow + b * 128;
     // P against the running max (the tile's own max on the first tile of the
-    // item, when O is still empty); rows whose values outgrew the running max
-    // by more than 2^8 (P > 256) are redone with their new max (rare)
+    // item, when O is still empty); rows whose tile sum outgrew the limit are
+    // redone with their new max (rare)
     if (j == 0) m_run = tile_max(sa, P.sl2, tile_valid);
-    float pmax;
-    float psum = softmax_pass_any(sa, P.sl2, m_run, tile_valid, pbuf, tid, &pmax);
-    const bool grow = pmax > kRescaleLimit;
+    float psum = softmax_pass_any(sa, P.sl2, m_run, tile_valid, pa);
+    const bool grow = psum > kRescaleSumLimit;
     if (j > 0 && __any_sync(0xffffffffu, grow)) {
-      if (!softmax_regrow(P, d, sa, trow, tile_valid, pbuf, g, grow, &m_run, &l_run, &psum))
+      if (!softmax_regrow(P, d, sa, trow, tile_valid, pa, g, grow, &m_run, &l_run, &psum))
         return;
     }
     l_run = (j == 0) ? psum : l_run + psum;
@@ -1177,35 +1403,49 @@ __device__ void softmax_item(const Params& P, DenseState& d, const Item& it, con
     if (tile_valid < kTileTok) {
       // rows past the chunk end may hold anything (even NaN): zero them in V
       // before PV reads them (0 * NaN would poison O)
-      if (!mbar_wait(bar_v(d, b), (g >> 1) & 1, d.abort)) return;
+      const uint32_t st = g % kStages;
+      if (!mbar_wait(bar_v(d, st), (g / kStages) & 1, d.abort)) return;
       if (tid >= tile_valid) {
-        uint8_t* vs = d.smem + kOffV + b * kTileBytes;
+        uint8_t* vs = d.smem + kOffV + st * kTileBytes;
 #pragma unroll
         for (int c = 0; c < 16; ++c)
           *reinterpret_cast<uint4*>(vs + (c >> 3) * kHalfBytes + tid * 128 + (c & 7) * 16) =
               make_uint4(0, 0, 0, 0);
       }
+      fence_proxy_async();
     }
-    fence_proxy_async();
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_p(d, b));
   }
-  // O is final once PV(last) is done.  A parity wait for phase k is only sound
-  // once phase k - 1 has completed (else it would read the pending phase k - 1
-  // as the completed phase k of the same parity); this warp has only seen
-  // PV(last - 2) complete so far, so PV(last - 1) is waited for first.
-  if (ntiles > 1 && !mbar_wait(bar_pv(d), (g0 + ntiles - 2) & 1, d.abort)) return;
+  // lane mu: member mu of this warp (its request, slots and ticket); the
+  // ticket is read now so that the read overlaps the wait for the last PV
+  const int mpw = 32 / P.G, src = (lane < mpw ? lane : 0) * P.G;
+  const int r_m = __shfl_sync(0xffffffffu, r_row, src);
+  const int sb_m = __shfl_sync(0xffffffffu, sb_row, src);
+  const int np_m = __shfl_sync(0xffffffffu, np_row, src);
+  uint32_t peek = 0;
+  if (lane < mpw && r_m >= 0) peek = ld_relaxed(&P.dp.tickets[(size_t)r_m * P.Hkv + it.kvh]);
+  // O is final once PV(last) is done; its commit on pfree of the last P
+  // buffer covers every earlier MMA too.  The wait is sound: that barrier's
+  // previous completion (PV(last - 2)) has happened and its next one needs
+  // this warp's P of the next item.  (A barrier that every PV completes would
+  // not do: PV(last) may complete before the warp first looks, and a wait for
+  // PV(last - 1) by parity then names a completion that never comes.)
   if (ntiles > 0) {
-    if (!mbar_wait(bar_pv(d), (g0 + ntiles - 1) & 1, d.abort)) return;
+    const uint32_t gl = g0 + ntiles - 1;
+    if (!mbar_wait(bar_pfree(d, gl & 1), (gl >> 1) & 1, d.abort)) return;
     tc_fence_after();
   }
 
-  // ---- epilogue.  O rows go through shared memory (the K/V stages are free
-  // now) so that each member's G rows leave as contiguous 512-byte rows and the
-  // merges read them back coalesced, lanes across d.
-  float* E = reinterpret_cast<float*>(d.smem + kOffK);     // [128][kEpiStride] fp32
-  float2* Eml = reinterpret_cast<float2*>(d.smem + kOffEml);  // [128] (m, l)
+  // ---- epilogue.  O rows go through shared memory so that each member's G
+  // rows leave as contiguous 512-byte rows and the merge reads them lanes
+  // across d.  E is [128][128] fp32 with float4 c of row t at position
+  // c ^ (t % 8): conflict-free for the row-per-thread writes and the
+  // row-at-a-time reads.
+  float* E = reinterpret_cast<float*>(d.smem + kOffE);
+  float2* Eml = reinterpret_cast<float2*>(d.smem + kOffEml);
+  fence_proxy_async();  // E overlays K stages the TMA and the tensor cores used
 #pragma unroll
   for (int q4 = 0; q4 < 4; ++q4) {
     float o[32];
@@ -1216,47 +1456,16 @@ __device__ void softmax_item(const Params& P, DenseState& d, const Item& it, con
       for (int e = 0; e < 32; ++e) o[e] = 0.f;
     }
 #pragma unroll
-    for (int e = 0; e < 32; e += 4)
-      *reinterpret_cast<float4*>(E + tid * kEpiStride + q4 * 32 + e) =
+    for (int e = 0; e < 32; e += 4) {
+      const int c = q4 * 8 + (e >> 2);
+      *reinterpret_cast<float4*>(E + tid * 128 + ((c ^ (tid & 7)) << 2)) =
           make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+    }
   }
   Eml[tid] = make_float2(m_run, l_run);
   tc_fence_before();
   __syncwarp();
-  // this warp's rows: 32 / G members of G rows each
-  const int mpw = 32 / G;
-  for (int mu = 0; mu < mpw; ++mu) {
-    const int row0 = warp * 32 + mu * G;
-    if (row0 >= nrows) break;
-    const int r = member_req(P, it, row0 / G);
-    const ReqInfo ri = P.dp.req[r];
-    float* dst = P.dp.opart + ((((size_t)ri.slot_base + it.slot_j) * P.Hkv + h) * G) * 128;
-    for (int x = lane; x < G * 32; x += 32) {  // G rows x 32 float4
-      const int rr = x >> 5, c = (x & 31) * 4;
-      __stcg(reinterpret_cast<float4*>(dst + rr * 128 + c),
-             *reinterpret_cast<const float4*>(E + (row0 + rr) * kEpiStride + c));
-    }
-    if (lane < G)
-      __stcg(&P.dp.mlpart[(((size_t)ri.slot_base + it.slot_j) * P.Hkv + h) * G + lane],
-             Eml[row0 + lane]);
-  }
-  __threadfence();
-  __syncwarp();
-  // tickets: lane mu takes the ticket of member mu of this warp
-  int last = 0;
-  int r_mine = -1;
-  if (lane < mpw && warp * 32 + lane * G < nrows) {
-    r_mine = member_req(P, it, (warp * 32 + lane * G) / G);
-    const ReqInfo ri = P.dp.req[r_mine];
-    uint32_t* ticket = &P.dp.tickets[(size_t)r_mine * P.Hkv + h];
-    last = atom_add_acq_rel(ticket, 1u) == (uint32_t)ri.n_partials - 1u;
-    if (last) st_relaxed(ticket, 0u);
-  }
-  uint32_t lastmask = __ballot_sync(0xffffffffu, last);
-  // merge the rows of every member whose last partial this was
-  if (lastmask) dense_merge_rows(P, it, h, nrows, lastmask);
-  // the staging buffer aliases the K/V stages the next item's TMA writes
-  fence_proxy_async();
+  dense_finish(P, it, d, E, Eml, nrows, r_m, sb_m, np_m, peek);
 }
 
 // Dense items of this CTA, run by warps 0-6 (224 threads).
@@ -1274,17 +1483,21 @@ __device__ void dense_loop(const Params& P, uint8_t* smem_raw) {
   d.abort = reinterpret_cast<volatile int*>(d.smem + kOffMisc + 16);
   if (control) {
     *d.abort = 0;
-    for (uint32_t st = 0; st < 2; ++st) {
+    for (uint32_t st = 0; st < (uint32_t)kStages; ++st) {
       mbar_init(bar_k(d, st), 1);
       mbar_init(bar_v(d, st), 1);
-      mbar_init(bar_s(d, st), 1);
-      mbar_init(bar_sfree(d, st), 4);
+      mbar_init(bar_kfree(d, st), 1);
+      mbar_init(bar_vfree(d, st), 1);
     }
-    mbar_init(bar_p(d, 0), 4);
-    mbar_init(bar_p(d, 1), 4);
-    mbar_init(bar_pv(d), 1);
-    mbar_init(bar_vfree(d, 0), 1);
-    mbar_init(bar_vfree(d, 1), 1);
+    for (uint32_t b = 0; b < 2; ++b) {
+      mbar_init(bar_s(d, b), 1);
+      mbar_init(bar_sfree(d, b), 4);
+      mbar_init(bar_p(d, b), 4);
+      mbar_init(bar_pfree(d, b), 1);
+    }
+    for (uint32_t k = 0; k < 8; ++k) mbar_init(d.sbase + kOffMergeBar + 8u * k, 1);
+    for (int w = 0; w < 4; ++w)
+      reinterpret_cast<volatile uint32_t*>(d.smem + kOffMisc + 32)[w] = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) {
@@ -1317,9 +1530,10 @@ __device__ void dense_loop(const Params& P, uint8_t* smem_raw) {
     }
     const int nb = (ntok + kBlockSize - 1) / kBlockSize;
     const int ntiles = (ntok + kTileTok - 1) / kTileTok;
-    if (tid < 128) prepare_item(P, d, it, nrows);
+    int r_row = -1;
+    if (tid < 128) r_row = prepare_item(P, d, it, nrows);
     dense_sync();
-    if (tid < 128) softmax_item(P, d, it, s, ntok, ntiles, nrows);
+    if (tid < 128) softmax_item(P, d, it, ntok, ntiles, nrows, r_row);
     else if (warp == 4) mma_item(P, d, ntiles);
     else if (warp == 5 || warp == 6) producer_item(P, d, s, it.kvh, warp - 5, nb, ntiles);
     tc_fence_before();

@@ -141,6 +141,16 @@ def test_dense_running_max_regrow():
     _check(p, *_run(p))
 
 
+def test_edge_dense_prefix_only_members():
+    """Members of a tensor-core group whose only partial is the prefix (no
+    suffix): the dense item's own partial is the whole output."""
+    _lib()
+    p = _custom(32, 8, 128, W.BF16, groups=[200, 1000], parent=None,
+                members=[0] * 10 + [1] * 9 + [-1],
+                suffix=[0, 0, 0, 5, 0, 17, 0, 0, 33, 0] + [0, 2, 0, 0, 0, 40, 0, 0, 1] + [7])
+    _check(p, *_run(p))
+
+
 def test_edge_three_level_chain():
     _lib()
     p = _custom(32, 8, 128, W.BF16, groups=[48, 20, 7, 100], parent=[-1, 0, 1, 0],
