@@ -215,7 +215,10 @@ int64_t psattn_plan_export(psattn_plan_t plan, int32_t which, int32_t* dst, int6
 /* Synchronises the device, reads and clears the kernel's error word.  Returns
  * PSATTN_OK, PSATTN_ERR_DEVICE (flags in *device_flags when non-NULL: 1 =
  * block id out of range, 2 = group_of_req differs from the plan, 4 = block
- * column beyond the table, 8 = a request with no token), or PSATTN_ERR_CUDA. */
+ * column beyond the table, 8 = a request with no token, 16 = a bounded wait
+ * inside the kernel gave up (the launch's results are incomplete), 32 = the
+ * merge bookkeeping found an inconsistency (more arrivals than partials, or a
+ * queued unit out of range)), or PSATTN_ERR_CUDA. */
 int psattn_plan_status(psattn_plan_t plan, uint32_t* device_flags);
 
 /* Frees the plan and its workspace (synchronises the device first).  NULL is a no-op. */

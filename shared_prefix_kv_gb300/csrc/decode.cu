@@ -83,12 +83,6 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
   return old;
 }
 
-__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
 __device__ __forceinline__ void st_relaxed(uint32_t* p, uint32_t v) {
   asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -685,18 +679,13 @@ constexpr int kStages = 3;                              // K and V ring depth
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kTileBytes;                  // kStages K stages
 constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;  // kStages V stages
-// Between items the stages are idle: the epilogue stages O ([128][128] fp32)
-// over the first two K stages and the merge buffers (4 warps x 32 KB) over the
-// rest.
+// between items the K stages hold the epilogue's O staging, [128][128] fp32
 constexpr uint32_t kOffE = kOffK;
-constexpr uint32_t kOffMergeBuf = kOffK + 2 * kTileBytes;
-constexpr uint32_t kOffEml = kOffV + kStages * kTileBytes;  // epilogue (m, l) of the 128 rows
-static_assert(kOffMergeBuf + 4 * 32768 <= kOffEml, "merge buffers overrun the stages");
+static_assert(128 * 128 * 4 <= kStages * kTileBytes, "O staging overruns the K stages");
 constexpr int kMaxDenseBlocks = 512;                    // chunk <= 8192 tokens
-constexpr uint32_t kOffBar = kOffEml + 128 * 8;         // 20 mbarriers
+constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;  // 20 mbarriers
 constexpr uint32_t kOffMisc = kOffBar + 160;
-constexpr uint32_t kOffMergeBar = kOffMisc + 64;        // 2 mbarriers per softmax warp
-constexpr uint32_t kDenseSmemBytes = kOffMergeBar + 64 + 1024;  // + alignment slack
+constexpr uint32_t kDenseSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
 static_assert(kDenseSmemBytes <= 232448, "dense tile shared memory exceeds 227 KB");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 256;                        // O accumulator columns
@@ -766,14 +755,6 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// bulk copy global -> shared (16-byte aligned, size a multiple of 16),
-// completion counted in bytes on an mbarrier
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
 
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -921,6 +902,12 @@ struct DenseState {
   uint32_t tmem;       // TMEM base address
   uint32_t g;          // tiles this CTA has run so far (drives every ring phase)
   volatile int* abort;
+  // softmax threads: the item's member tickets (lane mu: member mu's unit
+  // r * Hkv + h and partial count)
+  uint32_t pend_unit;
+  int pend_np;
+  int pend_valid;      // this lane has a member
+  int pend_any;        // the warp has tickets pending (same in every lane)
 };
 
 // mbarrier slots.  Tile g uses K/V stage g % kStages (completion number
@@ -1182,189 +1169,169 @@ __device__ __noinline__ bool softmax_regrow(const Params& P, DenseState& d, uint
   return true;
 }
 
-// End of a dense item for the 32 rows of the calling softmax warp (mpw = 32/G
-// members of G rows; O staged in E, (m, l) in Eml).  Lane mu speaks for member
-// mu (request r, partial slots from sb, np of them; peek = its ticket as read
-// before the last PV completed).  If the peek shows every other partial
-// already in, this item is the last one and merges straight from E without
-// writing its own partial; otherwise the member's rows go to its partial slot
-// and its ticket is taken, the last arriver merging.  The merge: lane = row
-// finds (M, 1/L) over the row's partials and writes the LSE; then each other
-// partial's rows come into a per-warp shared-memory buffer by cp.async (two
-// buffers, the next partial in flight while this one is added) and are added
-// into E lanes across d, a float4 per lane; E then leaves as bf16 rows.
-__device__ __noinline__ void dense_finish(const Params& P, const Item& it, DenseState& d, float* E,
-                                          const float2* Eml, int nrows, int r, int sb, int np,
-                                          uint32_t peek) {
-  constexpr uint32_t kAll = 0xffffffffu;
-  const int G = P.G, h = it.kvh, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mpw = 32 / G;
-  const bool valid = lane < mpw && warp * 32 + lane * G < nrows && r >= 0;
-  uint32_t* ticket = valid ? &P.dp.tickets[(size_t)r * P.Hkv + h] : nullptr;
-  const uint32_t need = (uint32_t)np - 1u;
-  const bool fast = valid && peek == need;
-  const uint32_t wmask = __ballot_sync(kAll, valid && !fast);
-  for (uint32_t m = wmask; m; m &= m - 1) {
-    const int mu = __ffs(m) - 1;
-    const int sbm = __shfl_sync(kAll, sb, mu);
-    const int row0 = warp * 32 + mu * G;
-    const size_t rix0 = (((size_t)sbm + it.slot_j) * P.Hkv + h) * G;
-    float* dst = P.dp.opart + rix0 * 128;
-    for (int x = lane; x < G * 32; x += 32) {
-      const int rr = x >> 5, c = x & 31, row = row0 + rr;
-      __stcg(reinterpret_cast<float4*>(dst + rr * 128 + c * 4),
-             *reinterpret_cast<const float4*>(E + row * 128 + ((c ^ (row & 7)) << 2)));
-    }
-    if (lane < G) __stcg(&P.dp.mlpart[rix0 + lane], Eml[row0 + lane]);
-  }
-  bool last = fast;
-  if (wmask) {
-    __threadfence();
-    __syncwarp();
-    if (valid && !fast) last = atom_add_acq_rel(ticket, 1u) == need;
-  }
-  if (last) st_relaxed(ticket, 0u);  // every partial is in: ready for the next launch
-  const uint32_t mmask = __ballot_sync(kAll, last);
-  if (!mmask) return;
-  __threadfence();  // with the ticket read above: the other partials are visible
+// ---- merge queue.  A dense item that turns out to be the last partial of a
+// (request, KV head) unit does not merge it: it puts the unit into its CTA's
+// ring in shared memory (r * Hkv + h + 1 per entry, 0 = empty) and moves on;
+// the CTA's other warps merge queued units between their own items, and every
+// warp drains the ring before the CTA ends.  `count` is claimed before an
+// entry is written or read, so head and tail never run more than a ring
+// apart; a writer still waits for its slot to be cleared (its previous reader
+// may not be done with it), and a reader for the entry to appear.  Both waits
+// are bounded.  A full ring makes the pushing warp merge the unit itself.
+constexpr int kMqCap = 256;
+struct MergeRing {
+  uint32_t e[kMqCap];
+  int count, head, tail;
+};
 
-  // lane = row: (M, 1/L) over the row's partials, every (m, l) load in flight
-  // at once; the weights of the first kNp partials stay in registers
-  constexpr int kNp = 8;
-  const int row = warp * 32 + lane, mu_r = lane / G, hl = lane % G;
-  const int sb_r = __shfl_sync(kAll, sb, mu_r);
-  const int np_r = __shfl_sync(kAll, np, mu_r);
-  const int r_r = __shfl_sync(kAll, r, mu_r);
-  const bool mrow = (mmask >> mu_r) & 1;
-  const size_t rstride = (size_t)P.Hkv * G;  // between slots of one row
-  const size_t rix_r = ((size_t)sb_r * P.Hkv + h) * G + hl;
-  float2 mlv[kNp];
+__device__ __forceinline__ bool ring_wait(volatile uint32_t* e, bool want_empty) {
+  const uint64_t t0 = global_ns();
+  while ((*e == 0u) != want_empty)
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  return true;
+}
+
+// By lane 0 of a warp whose lanes acquired the unit's partials (its ticket).
+__device__ bool mq_push(const Params& P, MergeRing& q, uint32_t unit) {
+  if (atomicAdd(&q.count, 1) >= kMqCap) {
+    atomicSub(&q.count, 1);
+    return false;
+  }
+  const int pos = atomicAdd(&q.tail, 1) & (kMqCap - 1);
+  volatile uint32_t* e = &q.e[pos];
+  if (!ring_wait(e, true)) {
+    raise(P, kErrTimeout);
+    return true;  // (the unit is lost; the error word says so)
+  }
+  __threadfence();  // the partials this thread acquired, before the entry
+  *e = unit + 1u;
+  return true;
+}
+
+// One unit from the ring, or -1 when it is empty (lane 0 claims, the warp gets
+// the answer).
+__device__ int mq_pop(const Params& P, MergeRing& q, int lane) {
+  int v = -1;
+  if (lane == 0) {
+    volatile int* cnt = &q.count;
+    int c = *cnt;
+    for (int tries = 0; c > 0; ++tries) {
+      if (tries > (1 << 20)) {  // never expected: the count keeps changing under it
+        raise(P, kErrMerge);
+        break;
+      }
+      if (atomicCAS(&q.count, c, c - 1) == c) {
+        const int pos = atomicAdd(&q.head, 1) & (kMqCap - 1);
+        volatile uint32_t* e = &q.e[pos];
+        if (ring_wait(e, false)) {
+          v = (int)*e - 1;
+          *e = 0u;
+        } else {
+          raise(P, kErrTimeout);
+        }
+        break;
+      }
+      c = *cnt;
+    }
+  }
+  v = __shfl_sync(0xffffffffu, v, 0);
+  if (v >= 0) __threadfence();  // with the pusher's fence: its partials are visible
+  return v;
+}
+
+// Merge of one queued unit (request r, KV head h), every partial read from the
+// partial store: four rows per round, lane = (row of the round, 16 values of
+// d), one online-softmax step per partial; output bf16 (queued units come
+// only from tensor-core items).  (Loading several partials per step before
+// combining them made the whole launch about twice as slow.)
+__device__ __noinline__ void merge_unit(const Params& P, int unit, int lane) {
+  const int G = P.G, r = unit / P.Hkv, h = unit % P.Hkv;
+  if (r < 0 || r >= P.R) {
+    if (lane == 0) raise(P, kErrMerge);
+    return;
+  }
+  const ReqInfo ri = P.dp.req[r];
+  const size_t jstride = (size_t)P.Hkv * G;
+  const int sub = lane >> 3, d0 = (lane & 7) * 16;
+  for (int r0 = 0; r0 < G; r0 += 4) {
+    const int hl = r0 + sub;
+    if (hl >= G) continue;
+    const size_t base = ((size_t)ri.slot_base * P.Hkv + h) * G + hl;
+    float acc[16];
 #pragma unroll
-  for (int j = 0; j < kNp; ++j)
-    mlv[j] = (mrow && j < np_r && j != it.slot_j) ? __ldcg(&P.dp.mlpart[rix_r + j * rstride])
-                                                   : make_float2(-INFINITY, 0.f);
-  float M = -INFINITY, inv = 0.f, wown = 0.f;
-  float wv[kNp];
-  if (mrow) {
-    const float2 own = Eml[row];
-    M = own.x;
+    for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+    float M = -INFINITY, L = 0.f;
+#pragma unroll 4
+    for (int j = 0; j < ri.n_partials; ++j) {
+      const size_t rix = base + j * jstride;
+      const float2 ml = __ldcg(&P.dp.mlpart[rix]);
+      const float4* src = reinterpret_cast<const float4*>(P.dp.opart + rix * 128 + d0);
+      float4 o[4];
 #pragma unroll
-    for (int j = 0; j < kNp; ++j) M = fmaxf(M, mlv[j].x);
-    for (int j = kNp; j < np_r; ++j)
-      if (j != it.slot_j) M = fmaxf(M, __ldcg(&P.dp.mlpart[rix_r + j * rstride]).x);
-    float L = own.x == -INFINITY ? 0.f : own.y * ex2(own.x - M);
+      for (int k = 0; k < 4; ++k) o[k] = __ldcg(src + k);
+      if (ml.x == -INFINITY) continue;
+      const float Mn = fmaxf(M, ml.x);
+      const float a = ex2(M - Mn), b = ex2(ml.x - Mn);
+      L = L * a + ml.y * b;
+      M = Mn;
 #pragma unroll
-    for (int j = 0; j < kNp; ++j)
-      if (mlv[j].x != -INFINITY) L += mlv[j].y * ex2(mlv[j].x - M);
-    for (int j = kNp; j < np_r; ++j) {
-      if (j == it.slot_j) continue;
-      const float2 ml = __ldcg(&P.dp.mlpart[rix_r + j * rstride]);
-      if (ml.x != -INFINITY) L += ml.y * ex2(ml.x - M);
+      for (int k = 0; k < 4; ++k) {
+        acc[4 * k] = acc[4 * k] * a + o[k].x * b;
+        acc[4 * k + 1] = acc[4 * k + 1] * a + o[k].y * b;
+        acc[4 * k + 2] = acc[4 * k + 2] * a + o[k].z * b;
+        acc[4 * k + 3] = acc[4 * k + 3] * a + o[k].w * b;
+      }
     }
     const bool empty = !(L > 0.f);
-    inv = empty ? 0.f : 1.f / L;
-    wown = (empty || own.x == -INFINITY) ? 0.f : ex2(own.x - M) * inv;
-    if (empty) raise(P, kErrEmpty);
-    if (P.lse) P.lse[(size_t)r_r * P.Hq + h * G + hl] = empty ? -INFINITY : (M + __log2f(L)) * kLn2;
-  }
+    const float inv = empty ? 0.f : 1.f / L;
 #pragma unroll
-  for (int j = 0; j < kNp; ++j) wv[j] = mlv[j].x == -INFINITY ? 0.f : ex2(mlv[j].x - M) * inv;
-
-  const uint32_t rmask = __ballot_sync(kAll, mrow);
-  const int jmax = __reduce_max_sync(kAll, mrow ? np_r : 0);
-  // E row of a merged row, scaled by the row's own weight
-  for (uint32_t m = rmask; m; m &= m - 1) {
-    const int rl = __ffs(m) - 1, rw = warp * 32 + rl;
-    const float w = __shfl_sync(kAll, wown, rl);
-    float4* e = reinterpret_cast<float4*>(E + rw * 128 + ((lane ^ (rw & 7)) << 2));
-    const float4 v = *e;
-    *e = make_float4(v.x * w, v.y * w, v.z * w, v.w * w);
-  }
-  // (rows with no partial but this one: E is already the output)
-  if (jmax > (it.slot_j == 0 ? 1 : 0)) {
-    // The other partials come in by bulk copy, one G-row block (contiguous in
-    // the partial store) per member, into two [32][128] fp32 buffers per warp in
-    // the idle K/V stages, each with its mbarrier.
-    const uint32_t buf0 = d.sbase + kOffMergeBuf + warp * (2u * 32 * 128 * 4);
-    const uint32_t mb0 = d.sbase + kOffMergeBar + warp * 16u;
-    // bit bi: parity of buffer bi's next completion (kept across items)
-    volatile uint32_t* phase_word = reinterpret_cast<volatile uint32_t*>(d.smem + kOffMisc + 32) + warp;
-    uint32_t phase = *phase_word;
-    fence_proxy_async();
-    __syncwarp();
-    auto issue = [&](int j, int bi) {
-      const bool cp = valid && ((mmask >> lane) & 1) && j < np && j != it.slot_j;
-      const uint32_t n = __popc(__ballot_sync(kAll, cp));
-      const uint32_t bar = mb0 + 8u * bi;
-      if (lane == 0) mbar_expect_tx(bar, n * (uint32_t)G * 512u);
-      __syncwarp();
-      if (cp)
-        bulk_g2s(buf0 + (uint32_t)bi * (32u * 128 * 4) + (uint32_t)(lane * G) * 512u,
-                 P.dp.opart + ((((size_t)sb + j) * P.Hkv + h) * G) * 128, (uint32_t)G * 512u, bar);
-    };
-    // E rows += w (this lane's row weight) x buffer bi, once its copies are in
-    auto accumulate = [&](float wl, int bi) -> bool {
-      if (!mbar_wait(mb0 + 8u * bi, (phase >> bi) & 1, d.abort)) return false;
-      phase ^= 1u << bi;
-      const float* bj = reinterpret_cast<const float*>(d.smem + kOffMergeBuf) + warp * (2 * 32 * 128) +
-                        bi * (32 * 128);
-      for (uint32_t m = rmask; m; m &= m - 1) {
-        const int rl = __ffs(m) - 1, rw = warp * 32 + rl;
-        const float w = __shfl_sync(kAll, wl, rl);
-        if (w != 0.f) {  // (an empty partial, or one past the row's count, adds nothing)
-          float4* e = reinterpret_cast<float4*>(E + rw * 128 + ((lane ^ (rw & 7)) << 2));
-          const float4 o = *reinterpret_cast<const float4*>(bj + rl * 128 + lane * 4);
-          float4 v = *e;
-          v.x += w * o.x; v.y += w * o.y; v.z += w * o.z; v.w += w * o.w;
-          *e = v;
-        }
-      }
-      // the buffer is read: the next bulk copy into it may start
-      fence_proxy_async();
-      __syncwarp();
-      return true;
-    };
-    auto next_j = [&](int j) { return (j + 1 == it.slot_j) ? j + 2 : j + 1; };
-    // two-deep pipeline: partial j is added while the next one is in flight
-    int bi = 0;
-    issue(it.slot_j == 0 ? 1 : 0, 0);
-    auto step = [&](int j, float wl) -> bool {
-      const int jn = next_j(j);
-      if (jn < jmax) issue(jn, bi ^ 1);
-      if (!accumulate(wl, bi)) return false;
-      bi ^= 1;
-      return true;
-    };
-#pragma unroll
-    for (int j = 0; j < kNp; ++j)
-      if (j < jmax && j != it.slot_j && !step(j, wv[j])) return;
-    for (int j = kNp; j < jmax; ++j) {  // rows with more partials: weights from (m, l) again
-      if (j == it.slot_j) continue;
-      float wl = 0.f;
-      if (mrow && j < np_r) {
-        const float2 ml = __ldcg(&P.dp.mlpart[rix_r + j * rstride]);
-        wl = ml.x == -INFINITY ? 0.f : ex2(ml.x - M) * inv;
-      }
-      if (!step(j, wl)) return;
+    for (int e = 0; e < 16; ++e) acc[e] *= inv;
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(P.out) + ((size_t)r * P.Hq + h * G + hl) * 128 + d0;
+    store_out<__nv_bfloat16>(out, acc, 8);
+    store_out<__nv_bfloat16>(out + 8, acc + 8, 8);
+    if ((lane & 7) == 0) {
+      if (empty) raise(P, kErrEmpty);
+      if (P.lse) P.lse[(size_t)r * P.Hq + h * G + hl] = empty ? -INFINITY : (M + __log2f(L)) * kLn2;
     }
-    if (lane == 0) *phase_word = phase;
   }
-  // the merged rows leave as bf16
-  for (uint32_t m = rmask; m; m &= m - 1) {
-    const int rl = __ffs(m) - 1, rw = warp * 32 + rl;
-    const int rq = __shfl_sync(kAll, r_r, rl);
-    const float4 v = *reinterpret_cast<const float4*>(E + rw * 128 + ((lane ^ (rw & 7)) << 2));
-    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(P.out) +
-                         ((size_t)rq * P.Hq + h * G + rl % G) * 128 + lane * 4;
-    *reinterpret_cast<uint2*>(out) = make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
+}
+
+// The member tickets of the softmax warp's item, once its partial rows are
+// written (lane mu: member mu).  The last arriver of a unit queues its merge;
+// a full ring makes the warp merge it here.  (Taking the tickets a tile into
+// the next item instead, to hide the fence, was tried: a launch then
+// occasionally never finished, and no bounded wait fired; see the design
+// notes.)
+__device__ void settle_tickets(const Params& P, DenseState& d, MergeRing& ring) {
+  const int lane = threadIdx.x & 31;
+  __threadfence();
+  __syncwarp();
+  bool last = false;
+  if (d.pend_valid) {
+    uint32_t* ticket = &P.dp.tickets[d.pend_unit];
+    const uint32_t old = atom_add_acq_rel(ticket, 1u);
+    if (old >= (uint32_t)d.pend_np) raise(P, kErrMerge);  // more arrivals than partials
+    last = old == (uint32_t)d.pend_np - 1u;
+    if (last) st_relaxed(ticket, 0u);  // every partial is in: ready for the next launch
+  }
+  d.pend_valid = 0;
+  d.pend_any = 0;
+  const uint32_t lastmask = __ballot_sync(0xffffffffu, last);
+  if (lastmask) __threadfence();  // the acquiring lanes' view, for the whole warp
+  for (uint32_t m = lastmask; m; m &= m - 1) {
+    const int mu = __ffs(m) - 1;
+    const uint32_t unit = __shfl_sync(0xffffffffu, d.pend_unit, mu);
+    int ok = 1;
+    if (lane == 0) ok = mq_push(P, ring, unit);
+    if (!__shfl_sync(0xffffffffu, ok, 0)) merge_unit(P, (int)unit, lane);  // ring full
   }
 }
 
 // The softmax warps' part of one item, then the epilogue.  r_row is the
 // request of this thread's row (-1 past the item's rows).  Returns early
 // (abort set) on a timeout.
-__device__ void softmax_item(const Params& P, DenseState& d, const Item& it, int ntok, int ntiles,
-                             int nrows, int r_row) {
+__device__ void softmax_item(const Params& P, DenseState& d, MergeRing& ring, const Item& it,
+                             int ntok, int ntiles, int nrows, int r_row) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t g0 = d.g;
   const uint32_t trow = d.tmem + ((uint32_t)(warp * 32) << 16);
@@ -1418,14 +1385,6 @@ __device__ void softmax_item(const Params& P, DenseState& d, const Item& it, int
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_p(d, b));
   }
-  // lane mu: member mu of this warp (its request, slots and ticket); the
-  // ticket is read now so that the read overlaps the wait for the last PV
-  const int mpw = 32 / P.G, src = (lane < mpw ? lane : 0) * P.G;
-  const int r_m = __shfl_sync(0xffffffffu, r_row, src);
-  const int sb_m = __shfl_sync(0xffffffffu, sb_row, src);
-  const int np_m = __shfl_sync(0xffffffffu, np_row, src);
-  uint32_t peek = 0;
-  if (lane < mpw && r_m >= 0) peek = ld_relaxed(&P.dp.tickets[(size_t)r_m * P.Hkv + it.kvh]);
   // O is final once PV(last) is done; its commit on pfree of the last P
   // buffer covers every earlier MMA too.  The wait is sound: that barrier's
   // previous completion (PV(last - 2)) has happened and its next one needs
@@ -1438,19 +1397,19 @@ __device__ void softmax_item(const Params& P, DenseState& d, const Item& it, int
     tc_fence_after();
   }
 
-  // ---- epilogue.  O rows go through shared memory so that each member's G
-  // rows leave as contiguous 512-byte rows and the merge reads them lanes
-  // across d.  E is [128][128] fp32 with float4 c of row t at position
-  // c ^ (t % 8): conflict-free for the row-per-thread writes and the
-  // row-at-a-time reads.
+  // ---- epilogue.  O rows go through shared memory (the K stages are idle
+  // until the next item) so that each member's G rows leave as contiguous
+  // 512-byte rows, lanes across d.  E is [128][128] fp32 with float4 c of row
+  // t at position c ^ (t % 8): conflict-free for the row-per-thread writes
+  // and the row-at-a-time reads.
+  const int G = P.G, h = it.kvh;
   float* E = reinterpret_cast<float*>(d.smem + kOffE);
-  float2* Eml = reinterpret_cast<float2*>(d.smem + kOffEml);
   fence_proxy_async();  // E overlays K stages the TMA and the tensor cores used
 #pragma unroll
   for (int q4 = 0; q4 < 4; ++q4) {
     float o[32];
     if (ntiles > 0) {
-      tmem_ld32(trow + kTmemO + q4 * 32, o);
+      tmem_ld32(trow + kTmemO + q4 * 32, o);  // warp-collective: every lane
     } else {
 #pragma unroll
       for (int e = 0; e < 32; ++e) o[e] = 0.f;
@@ -1462,14 +1421,37 @@ __device__ void softmax_item(const Params& P, DenseState& d, const Item& it, int
           make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
     }
   }
-  Eml[tid] = make_float2(m_run, l_run);
+  if (tid < nrows && r_row >= 0)
+    __stcg(&P.dp.mlpart[(((size_t)sb_row + it.slot_j) * P.Hkv + h) * G + tid % G],
+           make_float2(m_run, l_run));
   tc_fence_before();
   __syncwarp();
-  dense_finish(P, it, d, E, Eml, nrows, r_m, sb_m, np_m, peek);
+  // this warp's members: lane mu speaks for member mu (rows warp * 32 + mu * G ..)
+  const int mpw = 32 / G, src = (lane < mpw ? lane : 0) * G;
+  const int sb_m = __shfl_sync(0xffffffffu, sb_row, src);
+  for (int mu = 0; mu < mpw; ++mu) {
+    const int row0 = warp * 32 + mu * G;
+    if (row0 >= nrows) break;
+    const int sbm = __shfl_sync(0xffffffffu, sb_m, mu);
+    float* dst = P.dp.opart + ((((size_t)sbm + it.slot_j) * P.Hkv + h) * G) * 128;
+    for (int x = lane; x < G * 32; x += 32) {
+      const int rr = x >> 5, c = x & 31, row = row0 + rr;
+      __stcg(reinterpret_cast<float4*>(dst + rr * 128 + c * 4),
+             *reinterpret_cast<const float4*>(E + row * 128 + ((c ^ (row & 7)) << 2)));
+    }
+  }
+  // lane mu takes member mu's ticket; the last arriver of a unit queues its merge
+  const int r_m = __shfl_sync(0xffffffffu, r_row, src);
+  const int np_m = __shfl_sync(0xffffffffu, np_row, src);
+  d.pend_valid = lane < mpw && warp * 32 + lane * G < nrows && r_m >= 0;
+  d.pend_unit = (uint32_t)(d.pend_valid ? r_m : 0) * P.Hkv + h;
+  d.pend_np = np_m;
+  d.pend_any = 1;
+  settle_tickets(P, d, ring);
 }
 
 // Dense items of this CTA, run by warps 0-6 (224 threads).
-__device__ void dense_loop(const Params& P, uint8_t* smem_raw) {
+__device__ void dense_loop(const Params& P, uint8_t* smem_raw, MergeRing& ring) {
   const int tid = threadIdx.x, warp = tid >> 5;
   const bool control = (tid == 128);
   DenseState d;
@@ -1478,6 +1460,10 @@ __device__ void dense_loop(const Params& P, uint8_t* smem_raw) {
   d.smem = smem_raw + pad;
   d.sbase = raw + pad;
   d.g = 0;
+  d.pend_unit = 0;
+  d.pend_np = 0;
+  d.pend_valid = 0;
+  d.pend_any = 0;
   volatile int* s_idx = reinterpret_cast<volatile int*>(d.smem + kOffMisc);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(d.smem + kOffMisc + 8);
   d.abort = reinterpret_cast<volatile int*>(d.smem + kOffMisc + 16);
@@ -1495,9 +1481,6 @@ __device__ void dense_loop(const Params& P, uint8_t* smem_raw) {
       mbar_init(bar_p(d, b), 4);
       mbar_init(bar_pfree(d, b), 1);
     }
-    for (uint32_t k = 0; k < 8; ++k) mbar_init(d.sbase + kOffMergeBar + 8u * k, 1);
-    for (int w = 0; w < 4; ++w)
-      reinterpret_cast<volatile uint32_t*>(d.smem + kOffMisc + 32)[w] = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) {
@@ -1533,7 +1516,7 @@ __device__ void dense_loop(const Params& P, uint8_t* smem_raw) {
     int r_row = -1;
     if (tid < 128) r_row = prepare_item(P, d, it, nrows);
     dense_sync();
-    if (tid < 128) softmax_item(P, d, it, ntok, ntiles, nrows, r_row);
+    if (tid < 128) softmax_item(P, d, ring, it, ntok, ntiles, nrows, r_row);
     else if (warp == 4) mma_item(P, d, ntiles);
     else if (warp == 5 || warp == 6) producer_item(P, d, s, it.kvh, warp - 5, nb, ntiles);
     tc_fence_before();
@@ -1571,9 +1554,25 @@ __device__ __forceinline__ void run_item(const Params& P, const Item& it, int la
 template <int PATH>
 __global__ void __launch_bounds__(kThreads, 1) psattn_fused_decode(const __grid_constant__ Params P) {
   const int lane = threadIdx.x & 31;
-  if constexpr (PATH == kPathMmaBf16D128) {
+  // tensor-core items run (and may queue merges) while s_dense_active is set
+  __shared__ volatile int s_dense_active;
+  __shared__ MergeRing ring;
+  constexpr bool kMma = PATH == kPathMmaBf16D128;
+  const bool queue = kMma && P.dp.n_ditems > 0;
+  if constexpr (kMma) {
     extern __shared__ uint8_t dyn_smem[];
-    if (P.dp.n_ditems > 0 && threadIdx.x < kDenseThreads) dense_loop(P, dyn_smem);
+    if (queue) {
+      for (int i = threadIdx.x; i < kMqCap; i += blockDim.x) ring.e[i] = 0u;
+      if (threadIdx.x == 0) {
+        ring.count = ring.head = ring.tail = 0;
+        s_dense_active = 1;
+      }
+      __syncthreads();
+      if (threadIdx.x < kDenseThreads) {
+        dense_loop(P, dyn_smem, ring);
+        if (threadIdx.x == 0) s_dense_active = 0;
+      }
+    }
   }
   for (;;) {
     int idx = 0;
@@ -1584,6 +1583,28 @@ __global__ void __launch_bounds__(kThreads, 1) psattn_fused_decode(const __grid_
     const int4 a = __ldg(ip), b = __ldg(ip + 1);
     const Item it{a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
     run_item<PATH>(P, it, lane);
+    if (queue) {  // the queued merges, between items
+      for (int u = mq_pop(P, ring, lane); u >= 0; u = mq_pop(P, ring, lane)) merge_unit(P, u, lane);
+    }
+  }
+  if (queue) {
+    // Drain the ring.  While this CTA's tensor-core items run, more merges may
+    // come (sleep between looks); once they are done, empty means done.
+    uint64_t t0 = global_ns();
+    for (;;) {
+      const int u = mq_pop(P, ring, lane);
+      if (u >= 0) {
+        merge_unit(P, u, lane);
+        t0 = global_ns();
+        continue;
+      }
+      if (!s_dense_active) break;
+      if (global_ns() - t0 > kWaitLimitNs) {  // the CTA's tensor-core items never finished
+        if (lane == 0) raise(P, kErrTimeout);
+        break;
+      }
+      __nanosleep(1000);
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0) {

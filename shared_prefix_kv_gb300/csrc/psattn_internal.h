@@ -61,7 +61,7 @@ static_assert(sizeof(GroupInfo) == 32, "GroupInfo layout");
 
 // Device error-word flags.
 enum : uint32_t { kErrBlockOob = 1u, kErrGroup = 2u, kErrColumn = 4u, kErrEmpty = 8u,
-                  kErrTimeout = 16u };
+                  kErrTimeout = 16u, kErrMerge = 32u };
 
 // Counter words at the head of the workspace.
 enum : int { kCtrWarp = 0, kCtrDense = 1, kCtrExit = 2, kCtrErr = 3, kCtrWords = 8 };
