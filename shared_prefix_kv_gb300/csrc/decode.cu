@@ -646,11 +646,13 @@ __device__ __forceinline__ void simt_item(const Params& P, const Item& it, int l
 // A dense item is (group, KV head, chunk of the group's level, up to 128/G
 // members): 128 rows of q (member x q head of the KV head; padding rows are
 // zero) against the chunk's K/V, read once for all rows (the prefix partial as
-// a matrix product, BatchLLM section 2.2).  Seven warps of the CTA run it:
+// a matrix product, BatchLLM section 2.2).  Eight warps of the CTA run it:
 //
 //   warps 0-3   softmax and epilogue, thread t owning row t (= TMEM lane t);
-//   warp 4      lane 0 issues every tcgen05 MMA and commit;
-//   warps 5, 6  TMA producers of the K and the V tiles.
+//   warp 4      lane 0 issues the S = Q K^T MMAs and their commits;
+//   warps 5, 6  TMA producers of the K and the V tiles;
+//   warp 7      lane 0 issues the PV MMAs and their commits.
+// Warps 8-11 run per-warp items meanwhile (one per SM sub-partition).
 //
 // For each 128-token tile g (counted across items, so the rings continue):
 //   TMA       K(g), V(g): 8 paged blocks x 2 halves of d, 128B-swizzled boxes
@@ -667,8 +669,8 @@ __device__ __forceinline__ void simt_item(const Params& P, const Item& it, int l
 //   PV(g)     O += P V(g), P as the A operand straight from TMEM, V as the
 //             MN-major B operand from shared memory, fp32 in TMEM columns
 //             256-383.
-// The MMA warp issues S(g + 1) while the softmax works on S(g), so the tensor
-// core and the softmax overlap.  Every wait is bounded: on a timeout the CTA
+// S(g + 1) is issued while the softmax works on S(g), so the tensor core and
+// the softmax overlap.  Every wait is bounded: on a timeout the CTA
 // raises the error word, sets an abort flag that makes every later wait
 // return at once, and leaves its dense work.
 
@@ -699,7 +701,7 @@ constexpr uint32_t kTmemP = 384;                        // two P buffers of 64 c
 #endif
 constexpr float kRescaleSumLimit = (float)(1u << PSATTN_RESCALE_LOG2_SUM);
 constexpr uint64_t kWaitLimitNs = 2000000000ull;        // 2 s per wait
-constexpr int kDenseThreads = 224;                      // warps 0-6
+constexpr int kDenseThreads = 256;                      // warps 0-7
 
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -760,9 +762,9 @@ __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// named barrier 1 over the 224 threads of warps 0-6 (the dense group)
+// named barrier 1 over the 256 threads of warps 0-7 (the dense group)
 // (non-aligned form: lanes of the MMA and producer warps may arrive apart)
-__device__ __forceinline__ void dense_sync() { asm volatile("barrier.sync 1, 224;" ::: "memory"); }
+__device__ __forceinline__ void dense_sync() { asm volatile("barrier.sync 1, 256;" ::: "memory"); }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
                                             uint32_t bar) {
@@ -969,57 +971,58 @@ __device__ __forceinline__ void issue_kv(const Params& P, const DenseState& d, i
   }
 }
 
-// The MMA warp's part of one item (warp 4; lane 0 waits and issues):
-//   S(g) once K(g) has landed and the softmax is done with S(g - 2); commits
-//   to s[g % 2] and kfree[stage];
-//   PV(g - 1) once its P is written and its V has landed; commits to
-//   pfree[(g - 1) % 2] and vfree[stage].
-__device__ void mma_item(const Params& P, DenseState& d, int ntiles) {
-  const int lane = threadIdx.x & 31;
+// The tensor-core issue of one item, split over two threads so that neither
+// waits behind the other: issuing a tcgen05.mma blocks while the tensor core
+// is busy, and S(g + 1) should not queue behind PV(g - 1), which waits for
+// the slowest softmax warp.  (Commits track the committing thread's own
+// MMAs.)
+//   lane 0 of warp 4: S(g) once K(g) has landed and the softmax is done with
+//     S(g - 2); commits to s[g % 2] and kfree[stage].
+//   lane 0 of warp 7: PV(g) once P(g) is written and V(g) has landed;
+//     commits to pfree[g % 2] and vfree[stage].
+// Parity soundness (see mbar_wait): each thread saw the previous completion
+// of every barrier it waits on (its own earlier wait, or the previous item),
+// and the next completion needs an MMA it has not issued yet: K(g + 3) needs
+// kfree for S(g), sfree for S(g) needs S(g), V(g + 3) needs vfree for PV(g),
+// and P(g + 2) needs the softmax's wait for PV(g) (P buffer reuse).
+__device__ void mma_s_item(const Params& P, DenseState& d, int ntiles) {
+  if ((threadIdx.x & 31) != 0) return;
   const uint32_t g0 = d.g;
-  const uint32_t idesc_s = idesc_bf16_m128_n128(false), idesc_o = idesc_bf16_m128_n128(true);
+  const uint32_t idesc_s = idesc_bf16_m128_n128(false);
   const uint64_t qdesc = sw128_desc(d.sbase + kOffQ, 16, 1024);
-  auto wait0 = [&](uint32_t bar, uint32_t parity) -> bool {
-    int ok = 1;
-    if (lane == 0) ok = mbar_wait(bar, parity, d.abort);
-    return __shfl_sync(0xffffffffu, ok, 0) != 0;
-  };
-  auto pv = [&](uint32_t gp) -> bool {
-    const uint32_t st = gp % kStages;
-    if (!wait0(bar_p(d, gp & 1), (gp >> 1) & 1)) return false;
-    if (!wait0(bar_v(d, st), (gp / kStages) & 1)) return false;
-    if (lane == 0) {
-      tc_fence_after();
-      const uint64_t vdesc = sw128_desc(d.sbase + kOffV + st * kTileBytes, kHalfBytes, 1024);
-#pragma unroll
-      for (int k = 0; k < 8; ++k)  // 16 tokens of P = 8 TMEM columns per step
-        tc_mma_ta(d.tmem + kTmemO, d.tmem + kTmemP + (gp & 1) * 64 + k * 8,
-                  vdesc + ((k * 16 * 128) >> 4), idesc_o, (gp != g0 || k > 0));
-      tc_commit(bar_pfree(d, gp & 1));
-      tc_commit(bar_vfree(d, st));
-    }
-    __syncwarp();
-    return true;
-  };
   for (int j = 0; j < ntiles; ++j) {
     const uint32_t g = g0 + j, b = g & 1, st = g % kStages;
-    if (!wait0(bar_k(d, st), (g / kStages) & 1)) return;
-    if (g >= 2 && !wait0(bar_sfree(d, b), ((g >> 1) - 1) & 1)) return;
-    if (lane == 0) {
-      tc_fence_after();
-      const uint64_t kdesc = sw128_desc(d.sbase + kOffK + st * kTileBytes, 16, 1024);
+    if (!mbar_wait(bar_k(d, st), (g / kStages) & 1, d.abort)) return;
+    if (g >= 2 && !mbar_wait(bar_sfree(d, b), ((g >> 1) - 1) & 1, d.abort)) return;
+    tc_fence_after();
+    const uint64_t kdesc = sw128_desc(d.sbase + kOffK + st * kTileBytes, 16, 1024);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint32_t koff = ((k >> 2) * kHalfBytes + (k & 3) * 32) >> 4;
-        tc_mma(d.tmem + b * 128, qdesc + koff, kdesc + koff, idesc_s, k > 0);
-      }
-      tc_commit(bar_s(d, b));
-      tc_commit(bar_kfree(d, st));
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t koff = ((k >> 2) * kHalfBytes + (k & 3) * 32) >> 4;
+      tc_mma(d.tmem + b * 128, qdesc + koff, kdesc + koff, idesc_s, k > 0);
     }
-    __syncwarp();
-    if (j >= 1 && !pv(g - 1)) return;
+    tc_commit(bar_s(d, b));
+    tc_commit(bar_kfree(d, st));
   }
-  if (ntiles > 0) pv(g0 + ntiles - 1);
+}
+
+__device__ void mma_pv_item(const Params& P, DenseState& d, int ntiles) {
+  if ((threadIdx.x & 31) != 0) return;
+  const uint32_t g0 = d.g;
+  const uint32_t idesc_o = idesc_bf16_m128_n128(true);
+  for (int j = 0; j < ntiles; ++j) {
+    const uint32_t g = g0 + j, st = g % kStages;
+    if (!mbar_wait(bar_p(d, g & 1), (g >> 1) & 1, d.abort)) return;
+    if (!mbar_wait(bar_v(d, st), (g / kStages) & 1, d.abort)) return;
+    tc_fence_after();
+    const uint64_t vdesc = sw128_desc(d.sbase + kOffV + st * kTileBytes, kHalfBytes, 1024);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)  // 16 tokens of P = 8 TMEM columns per step
+      tc_mma_ta(d.tmem + kTmemO, d.tmem + kTmemP + (g & 1) * 64 + k * 8,
+                vdesc + ((k * 16 * 128) >> 4), idesc_o, (j > 0 || k > 0));
+    tc_commit(bar_pfree(d, g & 1));
+    tc_commit(bar_vfree(d, st));
+  }
 }
 
 // The producer warps' part of one item: warp 5 issues the K copies, warp 6
@@ -1450,7 +1453,7 @@ __device__ void softmax_item(const Params& P, DenseState& d, MergeRing& ring, co
   settle_tickets(P, d, ring);
 }
 
-// Dense items of this CTA, run by warps 0-6 (224 threads).
+// Dense items of this CTA, run by warps 0-7 (256 threads).
 __device__ void dense_loop(const Params& P, uint8_t* smem_raw, MergeRing& ring) {
   const int tid = threadIdx.x, warp = tid >> 5;
   const bool control = (tid == 128);
@@ -1517,7 +1520,8 @@ __device__ void dense_loop(const Params& P, uint8_t* smem_raw, MergeRing& ring) 
     if (tid < 128) r_row = prepare_item(P, d, it, nrows);
     dense_sync();
     if (tid < 128) softmax_item(P, d, ring, it, ntok, ntiles, nrows, r_row);
-    else if (warp == 4) mma_item(P, d, ntiles);
+    else if (warp == 4) mma_s_item(P, d, ntiles);
+    else if (warp == 7) mma_pv_item(P, d, ntiles);
     else if (warp == 5 || warp == 6) producer_item(P, d, s, it.kvh, warp - 5, nb, ntiles);
     tc_fence_before();
     dense_sync();
