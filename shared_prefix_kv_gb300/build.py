@@ -14,7 +14,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libpsattn.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["plan.cpp", "decode.cu", "noalloc.cu"]
+SOURCES = ["plan.cpp", "decode.cu", "noalloc.cu", "forest.cpp"]
 
 
 def _nvcc() -> str:
@@ -42,7 +42,8 @@ def _stale(obj: str, deps) -> bool:
 def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     os.makedirs(OUT, exist_ok=True)
     headers = [os.path.join(CSRC, h) for h in os.listdir(CSRC) if h.endswith(".h")]
-    headers.append(os.path.join(ROOT, "include", "psattn.h"))
+    headers += [os.path.join(ROOT, "include", h) for h in os.listdir(os.path.join(ROOT, "include"))
+                if h.endswith(".h")]
     objs, jobs = [], []
     for src in SOURCES:
         path = os.path.join(CSRC, src)

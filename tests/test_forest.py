@@ -1,0 +1,244 @@
+"""Prefix grouping from token ids (include/psattn_forest.h) against brute force.
+
+The checks are written from the definitions, independently of the library:
+  - multi-level groups: for every two requests, the levels on both chains add
+    up to their longest common prefix in whole chunks; each request's chain
+    ends at its longest prefix shared with any other request; the level tree
+    is compact (a level with one child level has a request ending at it);
+  - single level (BatchLLM section 4.2's first-level reuse): the saving equals
+    the maximum over every assignment of a shared chunk-prefix (or none) to
+    each request, enumerated exhaustively on tiny batches;
+  - batches (Feather's chunked hash tree, smallest miss count first): a
+    token-level simulation that recomputes every waiting request's misses at
+    every step gives the same batches and order.
+"""
+import itertools
+
+import numpy as np
+import pytest
+
+from shared_prefix_kv_gb300 import forest as F
+import shared_prefix_kv_gb300 as ps
+
+
+def lcp_chunks(a, b, chunk):
+    n = min(len(a) // chunk, len(b) // chunk)
+    c = 0
+    while c < n and list(a[c * chunk:(c + 1) * chunk]) == list(b[c * chunk:(c + 1) * chunk]):
+        c += 1
+    return c
+
+
+def chains(res):
+    """chain of levels (root first) of every request"""
+    out = []
+    for g in res["group_of_req"]:
+        ch = []
+        g = int(g)
+        while g >= 0:
+            ch.append(g)
+            g = int(res["group_parent"][g])
+        out.append(ch[::-1])
+    return out
+
+
+def random_batch(rng, R, chunk, alphabet=2, max_chunks=5, trunk=None):
+    """requests built from a few shared stems so that prefixes overlap"""
+    stems = [list(rng.integers(0, alphabet, size=rng.integers(0, max_chunks + 1) * chunk))
+             for _ in range(3)]
+    reqs = []
+    for _ in range(R):
+        s = stems[int(rng.integers(0, len(stems)))]
+        cut = int(rng.integers(0, len(s) // chunk + 1)) * chunk
+        tail = list(rng.integers(0, alphabet, size=int(rng.integers(0, 2 * chunk + 1))))
+        reqs.append((trunk or []) + s[:cut] + tail)
+    return reqs
+
+
+def check_multilevel(reqs, chunk):
+    res = F.forest_group(reqs, chunk=chunk)
+    R = len(reqs)
+    plen, gpar = res["prefix_len"], res["group_parent"]
+    ch = chains(res)
+    depth = [sum(int(plen[g]) for g in c) for c in ch]
+    for g in range(len(plen)):
+        assert plen[g] > 0 and plen[g] % chunk == 0
+        assert gpar[g] < g  # parents come first (depth-first numbering)
+    for i in range(R):
+        best = max([lcp_chunks(reqs[i], reqs[j], chunk) for j in range(R) if j != i] or [0])
+        assert depth[i] == best * chunk, (i, depth[i], best)
+        assert res["suffix_len"][i] == len(reqs[i]) - depth[i]
+        for j in range(i + 1, R):
+            common = sum(int(plen[g]) for g in set(ch[i]) & set(ch[j]))
+            assert common == lcp_chunks(reqs[i], reqs[j], chunk) * chunk, (i, j)
+    # compact: a level with exactly one child level has a request ending at it
+    kids = {g: [c for c in range(len(plen)) if gpar[c] == g] for g in range(len(plen))}
+    ends = set(int(g) for g in res["group_of_req"] if g >= 0)
+    for g in range(len(plen)):
+        assert len(kids[g]) != 1 or g in ends
+    through = [sum(1 for c in ch if g in c) for g in range(len(plen))]
+    assert res["saved_tokens"] == sum((through[g] - 1) * int(plen[g]) for g in range(len(plen)))
+    return res
+
+
+def brute_single(reqs, chunk):
+    """max over assignments of a chunk-prefix length (0 = none) to each request"""
+    opts = [range(len(r) // chunk + 1) for r in reqs]
+    best = 0
+    for pick in itertools.product(*opts):
+        groups = {}
+        for r, c in enumerate(pick):
+            if c:
+                groups.setdefault(tuple(reqs[r][:c * chunk]), []).append(r)
+        best = max(best, sum((len(m) - 1) * len(k) for k, m in groups.items()))
+    return best
+
+
+def check_single(reqs, chunk):
+    res = F.forest_group(reqs, chunk=chunk, single=True)
+    got = 0
+    for g, p in enumerate(res["prefix_len"]):
+        members = [r for r in range(len(reqs)) if res["group_of_req"][r] == g]
+        assert len(members) >= 2 and p > 0 and p % chunk == 0
+        stem = list(reqs[members[0]][:p])
+        assert all(list(reqs[r][:p]) == stem and len(reqs[r]) >= p for r in members)
+        got += (len(members) - 1) * int(p)
+    for r in range(len(reqs)):
+        g = int(res["group_of_req"][r])
+        assert res["suffix_len"][r] == len(reqs[r]) - (int(res["prefix_len"][g]) if g >= 0 else 0)
+    assert got == res["saved_tokens"]
+    return res
+
+
+def brute_cht(reqs, chunk, max_batch, max_new):
+    pre = [set(tuple(r[:c * chunk]) for c in range(1, len(r) // chunk + 1)) for r in reqs]
+    waiting = list(range(len(reqs)))
+    batch_of, order, nb = [0] * len(reqs), [], 0
+    while waiting:
+        seed = min(waiting)
+        waiting.remove(seed)
+        work = set(pre[seed])
+        batch_of[seed] = nb
+        order.append(seed)
+        size = 1
+        while size < max_batch and waiting:
+            m, r = min((len(pre[w] - work), w) for w in waiting)
+            if m > max_new:
+                break
+            waiting.remove(r)
+            work |= pre[r]
+            batch_of[r] = nb
+            order.append(r)
+            size += 1
+        nb += 1
+    return batch_of, order, nb
+
+
+# ---------------------------------------------------------------- examples
+
+def test_worked_example():
+    reqs = [[1, 2, 3, 4, 5, 6, 7, 8, 9], [1, 2, 3, 4, 5, 6, 0, 0], [1, 2, 3, 4, 9, 9, 9, 9, 1], [7, 7]]
+    res = check_multilevel(reqs, 2)
+    assert res["group_of_req"].tolist() == [1, 1, 0, -1]
+    assert res["group_parent"].tolist() == [-1, 0] and res["prefix_len"].tolist() == [4, 2]
+    assert res["saved_tokens"] == 2 * 4 + 1 * 2
+    single = check_single(reqs, 2)
+    assert single["saved_tokens"] == brute_single(reqs, 2) == 8  # all three at 4 tokens beat 2 at 6
+
+
+def test_enlargement_beats_the_deepest_level():
+    # two requests share 6 chunks, a third shares only the first 5 with them:
+    # grouping all three at 5 chunks saves 2 * 5 = 10 > 1 * 6
+    a = list(range(6))
+    reqs = [a + [7], a + [8], a[:5] + [9, 9]]
+    res = check_single(reqs, 1)
+    assert res["saved_tokens"] == 10 == brute_single(reqs, 1)
+    assert res["group_of_req"].tolist() == [0, 0, 0]
+
+
+def test_deeper_pair_kept_when_worth_more():
+    a = list(range(8))
+    reqs = [a + [1], a + [2], a[:2] + [5, 5]]
+    res = check_single(reqs, 1)  # pair at 8 saves 8 > all three at 2 (4)
+    assert res["saved_tokens"] == 8 == brute_single(reqs, 1)
+    assert res["group_of_req"].tolist() == [0, 0, -1]
+
+
+def test_edge_cases():
+    for reqs in ([], [[]], [[1, 2, 3]], [[1], [1]], [[5, 5, 5, 5]] * 4, [[], [1, 2], []]):
+        for chunk in (1, 2):
+            check_multilevel(reqs, chunk)
+            check_single(reqs, chunk)
+    res = F.forest_group([[3, 4, 5, 6]] * 3, chunk=2)
+    assert res["prefix_len"].tolist() == [4] and res["suffix_len"].tolist() == [0, 0, 0]
+    # a token past the last whole chunk is never shared
+    res = F.forest_group([[1, 2, 3], [1, 2, 3]], chunk=2)
+    assert res["prefix_len"].tolist() == [2] and res["suffix_len"].tolist() == [1, 1]
+
+
+def test_invalid_arguments():
+    tok, off = F.pack([[1, 2], [3]])
+    with pytest.raises(ps.PsattnError):
+        F.forest_group(tokens=tok, offsets=off, chunk=0)
+    with pytest.raises(ps.PsattnError):
+        F.forest_group(tokens=tok, offsets=np.array([0, 2, 1], np.int64), chunk=1)
+    with pytest.raises(ps.PsattnError):
+        F.cht_batches(tokens=tok, offsets=off, chunk=1, max_batch=0)
+
+
+# ------------------------------------------------------------ randomised
+
+@pytest.mark.parametrize("seed", range(40))
+def test_multilevel_random(seed):
+    rng = np.random.default_rng(seed)
+    chunk = int(rng.integers(1, 4))
+    check_multilevel(random_batch(rng, int(rng.integers(2, 12)), chunk), chunk)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_single_level_is_optimal(seed):
+    rng = np.random.default_rng(1000 + seed)
+    chunk = int(rng.integers(1, 3))
+    reqs = random_batch(rng, int(rng.integers(2, 6)), chunk, max_chunks=3)
+    res = check_single(reqs, chunk)
+    assert res["saved_tokens"] == brute_single(reqs, chunk)
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_cht_batches_match_brute_force(seed):
+    rng = np.random.default_rng(2000 + seed)
+    chunk = int(rng.integers(1, 4))
+    reqs = random_batch(rng, int(rng.integers(1, 14)), chunk)
+    max_batch = int(rng.integers(1, 6))
+    max_new = int(rng.integers(0, 4))
+    bor, order, nb = F.cht_batches(reqs, chunk=chunk, max_batch=max_batch, max_new_chunks=max_new)
+    exp_b, exp_o, exp_n = brute_cht(reqs, chunk, max_batch, max_new)
+    assert nb == exp_n and bor.tolist() == exp_b and order.tolist() == exp_o
+
+
+def test_forest_scales():
+    # 2000 requests under 16 system prompts with 4 few-shot variants each
+    rng = np.random.default_rng(7)
+    sys_p = [list(rng.integers(0, 50000, 256)) for _ in range(16)]
+    shots = [[list(rng.integers(0, 50000, 128)) for _ in range(4)] for _ in range(16)]
+    reqs, variant = [], []
+    for i in range(2000):
+        s, v = int(rng.integers(0, 16)), int(rng.integers(0, 4))
+        reqs.append(sys_p[s] + shots[s][v] + list(rng.integers(0, 50000, 40)))
+        variant.append(4 * s + v)
+    res = F.forest_group(reqs, chunk=16)
+    assert len(res["prefix_len"]) == 16 + 64
+    assert sorted(set(res["prefix_len"].tolist())) == [128, 256]
+    counts = np.bincount(variant, minlength=64)
+    per_sys = counts.reshape(16, 4).sum(axis=1)
+    assert res["saved_tokens"] == int(((per_sys - 1) * 256).sum() + ((counts - 1) * 128).sum())
+    # one level: each few-shot variant's ~31 requests at 384 tokens save more
+    # than its system prompt's ~125 at 256 (4 * 30 * 384 > 124 * 256)
+    single = F.forest_group(reqs, chunk=16, single=True)
+    assert single["saved_tokens"] == int(((counts - 1) * 384).sum())
+    assert sorted(set(single["prefix_len"].tolist())) == [384]
+    bor, order, nb = F.cht_batches(reqs, chunk=16, max_batch=128, max_new_chunks=0)
+    assert sorted(order.tolist()) == list(range(2000))
+    # with no new chunk allowed a batch holds one few-shot variant only
+    for b in range(nb):
+        assert len(set(np.asarray(variant)[bor == b].tolist())) == 1
