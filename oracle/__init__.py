@@ -75,6 +75,10 @@ def _load():
             lib.oracle_gather_kv.restype = ctypes.c_longlong
             lib.oracle_num_tokens.argtypes = [ctypes.POINTER(_Problem), ctypes.c_int]
             lib.oracle_num_tokens.restype = ctypes.c_longlong
+            lib.oracle_attention_chunked.argtypes = [ctypes.POINTER(_Problem), ctypes.c_void_p,
+                                                     ctypes.c_void_p, ctypes.c_void_p,
+                                                     ctypes.c_void_p, ctypes.c_int]
+            lib.oracle_attention_chunked.restype = ctypes.c_int
             lib.oracle_max_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -134,6 +138,27 @@ def attention(p, requests: Optional[Sequence[int]] = None, nthreads: int = 0):
                               n, out.ctypes.data, lse.ctypes.data, int(nthreads))
     if rc != 0:
         raise OracleError(f"oracle_attention failed with status {rc}")
+    return out, lse
+
+
+def attention_chunked(p, q_len, q, nthreads: int = 0):
+    """Chunked prefill: request r of problem `p` carries q_len[r] queries,
+    rows of `q` ([sum q_len][Hq][d], p's dtype) in request order; query i of
+    request r attends causally to the first n_tok - q_len[r] + i + 1 tokens of
+    its token list.  Returns (out [Q][Hq][d] float64, lse [Q][Hq] float64)."""
+    lib = _load()
+    m = _Marshalled(p)
+    ql = np.ascontiguousarray(q_len, dtype=np.int32)
+    qq = np.ascontiguousarray(q)
+    if ql.shape[0] != m.s.num_req or qq.shape[0] != int(ql.sum()):
+        raise OracleError("q_len / q rows do not match the problem")
+    n = qq.shape[0]
+    out = np.zeros((n, p.num_q_heads, p.head_dim), np.float64)
+    lse = np.zeros((n, p.num_q_heads), np.float64)
+    rc = lib.oracle_attention_chunked(ctypes.byref(m.s), ql.ctypes.data, qq.ctypes.data,
+                                      out.ctypes.data, lse.ctypes.data, int(nthreads))
+    if rc != 0:
+        raise OracleError(f"oracle_attention_chunked failed with status {rc}")
     return out, lse
 
 

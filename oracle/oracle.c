@@ -25,6 +25,14 @@
  *  - the decode token's own K/V is part of the suffix; no causal mask;
  *  - LSE is the natural log of sum(exp(scaled score)).
  *
+ * Chunked prefill (oracle_attention_chunked): BatchLLM (papercache.org,
+ * sections 2 and 6, chunked prefill / SplitFuse) mixes prefill chunks with
+ * decode tokens in one token batch.  Reading: a request's chunk of n queries
+ * is the last n tokens of its token list, and query i of the chunk attends to
+ * the tokens up to and including its own position (the causal mask of a
+ * decoder), i.e. the first n_tok - n + i + 1 tokens.  A decode request is a
+ * chunk of one query and sees every token, as above.
+ *
  * Arithmetic: inputs are widened exactly to double (bf16 -> fp32 -> double);
  * everything after that is double.  OpenMP spreads the (request, q head)
  * pairs over threads; each pair is computed independently, so the result
@@ -142,17 +150,19 @@ long long oracle_gather_kv(const oracle_problem* p, int r, int kvh, double* K, d
     return m;
 }
 
-/* Attention of one (request, q head) over all its tokens, from the definition. */
-static int attend_one(const oracle_problem* p, int r, int h, const int32_t* blk,
-                      const int32_t* slot, long long n, double* s, double* out, double* lse) {
+/* Attention of q row `qrow` of `q` ([rows][Hq][d]), head h, over the first n
+ * tokens of a request's token map, from the definition. */
+static int attend_one(const oracle_problem* p, const void* q, long long qrow, int h,
+                      const int32_t* blk, const int32_t* slot, long long n, double* s,
+                      double* out, double* lse) {
     const int d = p->head_dim;
     const int kvh = h / (p->num_q_heads / p->num_kv_heads);
-    const size_t qoff = ((size_t)r * p->num_q_heads + h) * d;
+    const size_t qoff = ((size_t)qrow * p->num_q_heads + h) * d;
     double m = -INFINITY;
     for (long long t = 0; t < n; ++t) {
         double acc = 0.0;
         for (int e = 0; e < d; ++e)
-            acc += widen(p->q, p->dtype, qoff + e) *
+            acc += widen(q, p->dtype, qoff + e) *
                    widen(p->pool, p->dtype, pool_index(p, blk[t], 0, kvh, slot[t], e));
         s[t] = acc * p->scale;
         if (s[t] > m) m = s[t];
@@ -226,11 +236,86 @@ int oracle_attention(const oracle_problem* p, const int32_t* req, int n_req, dou
                 }
                 cur = r;
             }
-            attend_one(p, r, h, blk, slot, ntok, s, out + ((size_t)k * Hq + h) * d,
+            attend_one(p, p->q, r, h, blk, slot, ntok, s, out + ((size_t)k * Hq + h) * d,
                        lse + (size_t)k * Hq + h);
         }
         free(blk); free(slot); free(s);
     }
+    return status;
+}
+
+/* Chunked prefill.  Request r has q_len[r] >= 1 queries; q is [Q][Hq][d] with
+ * Q = sum q_len, request r's queries at rows off_r .. off_r + q_len[r] - 1
+ * (off_r = sum of q_len over the earlier requests).  Query i of request r
+ * attends to the first n_tok(r) - q_len[r] + i + 1 tokens of r's token list.
+ * out: [Q][Hq][d] double, lse: [Q][Hq] double.  Returns 0 or a negative
+ * error (OR_BAD_ARG when a chunk is longer than its request's token list). */
+int oracle_attention_chunked(const oracle_problem* p, const int32_t* q_len, const void* q,
+                             double* out, double* lse, int nthreads) {
+    if (!p || !q_len || !q || p->num_q_heads <= 0 || p->num_kv_heads <= 0 ||
+        p->num_q_heads % p->num_kv_heads || p->head_dim <= 0 || p->block_size <= 0)
+        return OR_BAD_ARG;
+    const int R = p->num_req, Hq = p->num_q_heads, d = p->head_dim;
+    long long Q = 0;
+    for (int r = 0; r < R; ++r) {
+        if (q_len[r] < 1) return OR_BAD_ARG;
+        Q += q_len[r];
+    }
+    int32_t* req_of = (int32_t*)malloc(sizeof(int32_t) * (size_t)(Q ? Q : 1));
+    int32_t* idx_of = (int32_t*)malloc(sizeof(int32_t) * (size_t)(Q ? Q : 1));
+    long long k = 0;
+    for (int r = 0; r < R; ++r)
+        for (int i = 0; i < q_len[r]; ++i, ++k) {
+            req_of[k] = r;
+            idx_of[k] = i;
+        }
+    int status = OR_OK;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#endif
+#pragma omp parallel
+    {
+        long long cap = 0;
+        int32_t *blk = NULL, *slot = NULL;
+        double* s = NULL;
+        int cur = -1;
+        long long ntok = 0;
+#pragma omp for schedule(dynamic, 4)
+        for (long long i = 0; i < Q * Hq; ++i) {
+            const long long row = i / Hq;
+            const int h = (int)(i % Hq), r = req_of[row];
+            if (r != cur) {
+                long long need = oracle_num_tokens(p, r);
+                if (need < q_len[r]) {
+#pragma omp atomic write
+                    status = need < 0 ? (int)need : OR_BAD_ARG;
+                    cur = -1;
+                    continue;
+                }
+                if (need > cap) {
+                    free(blk); free(slot); free(s);
+                    cap = need;
+                    blk = (int32_t*)malloc(sizeof(int32_t) * (size_t)cap);
+                    slot = (int32_t*)malloc(sizeof(int32_t) * (size_t)cap);
+                    s = (double*)malloc(sizeof(double) * (size_t)cap);
+                }
+                ntok = token_map(p, r, blk, slot, cap);
+                if (ntok < 0) {
+#pragma omp atomic write
+                    status = (int)ntok;
+                    cur = -1;
+                    continue;
+                }
+                cur = r;
+            }
+            const long long nvis = ntok - q_len[r] + idx_of[row] + 1;
+            attend_one(p, q, row, h, blk, slot, nvis, s, out + ((size_t)row * Hq + h) * d,
+                       lse + (size_t)row * Hq + h);
+        }
+        free(blk); free(slot); free(s);
+    }
+    free(req_of);
+    free(idx_of);
     return status;
 }
 

@@ -23,6 +23,12 @@ MUTANTS = {
     "chain_leaf_first": ("for (int i = 0; i < n; ++i) out[i] = tmp[n - 1 - i];",
                          "for (int i = 0; i < n; ++i) out[i] = tmp[i];"),
     "weight_unnormalised": ("double w = s[t] / z;", "double w = s[t];"),
+    "causal_off_by_one": ("const long long nvis = ntok - q_len[r] + idx_of[row] + 1;",
+                          "const long long nvis = ntok - q_len[r] + idx_of[row];"),
+    "causal_no_mask": ("const long long nvis = ntok - q_len[r] + idx_of[row] + 1;",
+                       "const long long nvis = ntok;"),
+    "chunk_row_swap": ("attend_one(p, q, row, h, blk, slot, nvis,",
+                       "attend_one(p, q, (row + 1) % Q, h, blk, slot, nvis,"),
 }
 
 

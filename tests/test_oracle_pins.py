@@ -253,3 +253,81 @@ def test_oracle_never_reads_poison():
         p = W.make(name, small=True)
         out, lse = oracle.attention(p, list(range(0, p.num_req, 5)))
         assert np.isfinite(out).all() and np.isfinite(lse).all()
+
+
+# ---- chunked prefill (oracle.attention_chunked): query i of a chunk of n
+# queries attends to the first n_tok - n + i + 1 tokens of its request
+
+def _causal_dense(K, V, q, scale, n_q):
+    """K, V [Hkv][n][d] of one request, q [n_q][Hq][d] its chunk's queries."""
+    Hkv, n, _ = K.shape
+    Hq = q.shape[1]
+    G = Hq // Hkv
+    out = np.zeros(q.shape)
+    lse = np.zeros(q.shape[:2])
+    for i in range(n_q):
+        vis = n - n_q + i + 1
+        for h in range(Hq):
+            s = (K[h // G, :vis] @ q[i, h]) * scale
+            m = s.max()
+            w = np.exp(s - m)
+            out[i, h] = (w / w.sum()) @ V[h // G, :vis]
+            lse[i, h] = m + np.log(w.sum())
+    return out, lse
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_chunked_matches_dense_causal(seed):
+    rng = np.random.default_rng(500 + seed)
+    Hkv, G, d, B = 2, 2, 8, 4
+    P0 = int(rng.integers(0, 9))
+    levels = [(_rand_f32(rng, Hkv, P0, d), _rand_f32(rng, Hkv, P0, d))]
+    R = 4
+    sl = rng.integers(1, 12, R)
+    ql = np.array([int(rng.integers(1, s + 1)) for s in sl])
+    members = [int(rng.integers(-1, 1)) for _ in range(R)]
+    sufs = [(_rand_f32(rng, Hkv, s, d), _rand_f32(rng, Hkv, s, d)) for s in sl]
+    q_dec = _rand_f32(rng, R, Hkv * G, d)
+    p, dense = pack(levels, None, members, sufs, q_dec, Hkv=Hkv, B=B, seed=seed)
+    qc = _rand_f32(rng, int(ql.sum()), Hkv * G, d)
+    out, lse = oracle.attention_chunked(p, ql, qc.astype(np.float32))
+    row = 0
+    for r in range(R):
+        K, V = dense[r]
+        eo, el = _causal_dense(K, V, qc[row:row + ql[r]], p.scale, int(ql[r]))
+        np.testing.assert_allclose(out[row:row + ql[r]], eo, atol=1e-12, rtol=0)
+        np.testing.assert_allclose(lse[row:row + ql[r]], el, atol=1e-12, rtol=0)
+        row += ql[r]
+
+
+def test_chunked_one_query_is_decode():
+    p = W.make("skewed", small=True)
+    ones = np.ones(p.num_req, np.int32)
+    out, lse = oracle.attention_chunked(p, ones, p.q)
+    eo, el = oracle.attention(p)
+    assert np.array_equal(out, eo) and np.array_equal(lse, el)
+
+
+def test_chunked_first_query_sees_its_first_token():
+    # no prefix, the chunk is the whole suffix: query 0 sees token 0 only
+    rng = np.random.default_rng(3)
+    K = _rand_f32(rng, 1, 5, 4)
+    V = _rand_f32(rng, 1, 5, 4)
+    p = single_request(K, V, _rand_f32(rng, 1, 4), B=2)
+    qc = _rand_f32(rng, 5, 1, 4).astype(np.float32)
+    out, lse = oracle.attention_chunked(p, [5], qc)
+    assert np.array_equal(out[0, 0], V[0, 0])
+    assert lse[0, 0] == pytest.approx(float(qc[0, 0] @ K[0, 0]) * p.scale, abs=1e-13)
+    # the last query sees all five, as a decode query would
+    p.q = qc[4:5].copy()
+    eo, el = oracle.attention(p)
+    assert np.array_equal(out[4], eo[0]) and np.array_equal(lse[4], el[0])
+
+
+def test_chunked_rejects_chunk_longer_than_request():
+    p = W.make("tiny_fp32", small=True)
+    ql = np.ones(p.num_req, np.int32)
+    ql[0] = int(oracle.gather_kv(p, 0, 0)[0].shape[0]) + 1
+    with pytest.raises(oracle.OracleError):
+        oracle.attention_chunked(p, ql, np.zeros((int(ql.sum()), p.num_q_heads, p.head_dim),
+                                                 np.float32))
