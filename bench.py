@@ -49,6 +49,9 @@ DESCRIPTIONS = {
                  "64, suffix U[32,256], 3-partial merge, 32/8 heads, d 128, bf16",
     "two_level_flat": "the two-level workload flattened to one 5120-token level per group",
     "tiny_fp32": "2 groups x 8 requests, prefix 256, suffix U[1,64], 4/4 heads, d 64, fp32",
+    "chunked": "7 prefill chunks of U[256,512] queries beside 256 decode requests (8 groups x 32, "
+               "prefix 2048, suffix U[64,512]), 32/8 heads, d 128, bf16; chunks expanded into "
+               "decode rows with shared 128-token causal levels",
 }
 
 
@@ -67,9 +70,27 @@ def _peak_hbm():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def _traffic_record():
-    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
-    the current kernel source (else None)."""
+def _peak_bf16():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1900.0
+
+
+def _visible_tokens(p):
+    """Tokens each row attends to, summed over rows (prefix chain + suffix)."""
+    total = int(p.suffix_len.sum())
+    for r in range(p.num_req):
+        total += sum(int(p.prefix_len[g]) for g in p.chain(r))
+    return total
+
+
+def _traffic_record(workload):
+    """Per-launch DRAM bytes from the committed ncu summary of the Llama-3-8B
+    workload, if it was taken on the current kernel source (else None)."""
+    if workload != "llama8b":
+        return None
     src = os.path.join(ROOT, "shared_prefix_kv_gb300", "csrc", "decode.cu")
     path = os.path.join(ROOT, "profiles", "psattn_fused_decode_llama8b.md")
     try:
@@ -189,6 +210,32 @@ def _overrides(args):
     return {} if args.groups is None else {"n_groups": args.groups}
 
 
+def _make(args, seed=None):
+    """The workload's problem, and (algorithmic KV + q/out bytes, attention
+    FLOPs) when the bytes differ from what the plan reports (None otherwise).
+    A batch with prefill chunks runs as the library's expansion of it into
+    decode rows; its algorithmic bytes count each token of the original batch
+    once (a prefix once per group) plus q, out and lse of every query, and its
+    FLOPs are 4 * Hq * d per (query, visible token)."""
+    if args.workload != "chunked":
+        return W.make(args.workload, seed=seed, poison=False, **_overrides(args)), None
+    import dataclasses
+    import shared_prefix_kv_gb300 as ps
+    from shared_prefix_kv_gb300 import chunked
+    from workloads.device import shape_of
+    p, ql, q = W.make_chunked(seed=6 if seed is None else seed, poison=False)
+    sh, bt, gor, gpar, plen, slen = chunked.expand(shape_of(p), p.block_table, p.group_of_req,
+                                                   p.group_parent, p.prefix_len, p.suffix_len,
+                                                   ql, 128)
+    p2 = dataclasses.replace(p, q=q, block_table=bt, group_of_req=gor, group_parent=gpar,
+                             prefix_len=plen, suffix_len=slen)
+    used = sorted(set(int(g) for g in p.group_of_req) - {-1})
+    tok = sum(int(p.prefix_len[g]) for g in used) + int(p.suffix_len.sum())
+    tb = 2 * p.num_kv_heads * p.head_dim * p.elem_bytes
+    qo = int(ql.sum()) * p.num_q_heads * (2 * p.head_dim * p.elem_bytes + 4)
+    return p2, (tok * tb + qo, 4.0 * p.num_q_heads * p.head_dim * _visible_tokens(p2))
+
+
 def _config(args, p):
     desc = DESCRIPTIONS.get(args.workload, args.workload)
     if args.groups is not None:
@@ -218,7 +265,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return 0
-        p = W.make(args.workload, poison=False, **_overrides(args))
+        p, _ = _make(args)
         return run_reference(args, p)
 
     import torch
@@ -232,8 +279,8 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
     # each rank gets its own independent batch (weak scaling)
-    p = W.make(args.workload, seed=None if rank == 0 else 1000 + rank, poison=False,
-               **_overrides(args))
+    p, chunk_info = _make(args, seed=None if rank == 0 else 1000 + rank)
+    alg_override = chunk_info[0] if chunk_info else None
     d = DeviceProblem(p)
     t_plan = time.perf_counter()
     plan = d.plan()
@@ -272,10 +319,10 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
     value = p.num_req * world / (ms * 1e-3)
-    alg_bytes = info["unique_kv_bytes"] + info["qo_bytes"]
+    alg_bytes = alg_override or (info["unique_kv_bytes"] + info["qo_bytes"])
     peak, peak_kind = _peak_hbm()
     achieved = alg_bytes / (ms * 1e-3) / 1e9
-    traffic = _traffic_record()
+    traffic = _traffic_record(args.workload)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -296,6 +343,10 @@ def main():
         "plan_ms": 1e3 * t_plan,
         "ms_per_step_median": float(np.median(times)),
     }
+    if chunk_info:  # prefill chunks make the batch heavy on the tensor cores too
+        tf = chunk_info[1] / (ms * 1e-3) / 1e12
+        line["tensor"] = {"flops_per_launch": chunk_info[1], "achieved_tflops": tf,
+                          "peak_tflops": _peak_bf16(), "frac": tf / _peak_bf16()}
 
     if not args.no_baselines:
         # same kernel, prefix de-duplication disabled

@@ -14,7 +14,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libpsattn.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["plan.cpp", "decode.cu", "noalloc.cu", "forest.cpp", "sched.cpp"]
+SOURCES = ["plan.cpp", "decode.cu", "noalloc.cu", "forest.cpp", "sched.cpp", "chunked.cpp"]
 
 
 def _nvcc() -> str:

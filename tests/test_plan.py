@@ -297,12 +297,13 @@ def test_status_strings():
 
 
 def test_abi_exports_every_declared_symbol():
-    from shared_prefix_kv_gb300 import forest, sched
+    from shared_prefix_kv_gb300 import chunked, forest, sched
     inc = os.path.dirname(ROOT_HEADER)
     text = "".join(open(os.path.join(inc, h)).read() for h in sorted(os.listdir(inc))
                    if h.endswith(".h"))
     declared = set(re.findall(r"^\s*(?:int|int64_t|void|const char\*)\s+(psattn_\w+)\s*\(",
                               text, flags=re.M))
-    assert declared >= set(ps.EXPORTED_SYMBOLS) | set(forest.EXPORTED_SYMBOLS) | set(sched.EXPORTED_SYMBOLS)
+    assert declared >= set(ps.EXPORTED_SYMBOLS) | set(forest.EXPORTED_SYMBOLS) | set(sched.EXPORTED_SYMBOLS) \
+        | set(chunked.EXPORTED_SYMBOLS)
     for name in declared:
         assert hasattr(ps._lib, name), name

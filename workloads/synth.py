@@ -312,6 +312,49 @@ def flatten_problem(p: Problem) -> Problem:
                                prefix_len=np.asarray(plen, np.int32), group_of_req=gor)
 
 
+def chunk_queries(p: Problem, q_len, stream_tag: int = 3) -> np.ndarray:
+    """q rows of a batch with prefill chunks: [sum q_len][Hq][d] in p's
+    storage dtype, N(0,1) (rounded to bf16 for bf16 problems), from p's seed
+    and a value stream of their own."""
+    n = int(np.sum(q_len))
+    store = np.float32 if p.dtype == F32 else np.uint16
+    q = np.empty((n, p.num_q_heads, p.head_dim), store)
+    _fill_normal(q.reshape(-1), p.dtype, p.seed, stream_tag)
+    return q
+
+
+def make_chunked(seed: int = 6, *, small: bool = False, poison: bool = True):
+    """Prefill chunks mixed with decode requests, Llama-3-8B attention shape
+    (bf16, 32/8 heads, d 128): the decode requests sit in groups under a shared
+    prompt; each prefill request joins one of those groups or none, has drawn
+    earlier distinct tokens, and a chunk of q_len new tokens at the end of its
+    suffix.  Full size: 8 groups x 32 decode requests (prefix 2048, suffix
+    uniform in [64, 512]) and 7 prefill requests (earlier tokens uniform in
+    [0, 1024], chunks uniform in [256, 512]).  Returns (Problem, q_len int32
+    [R], q [sum q_len][Hq][d])."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    if small:
+        ng, mem, prefix, dsuf, npre, early, chunk = 2, 8, 200, (1, 90), 3, (0, 70), (17, 100)
+    else:
+        ng, mem, prefix, dsuf, npre, early, chunk = 8, 32, 2048, (64, 512), 7, (0, 1024), (256, 512)
+    gor = [i // mem for i in range(ng * mem)]
+    slen = _uniform_int(rng, dsuf[0], dsuf[1], ng * mem)
+    ql = [1] * (ng * mem)
+    pre_g = rng.integers(-1, ng, size=npre).tolist()
+    pre_e = _uniform_int(rng, early[0], early[1], npre)
+    pre_c = _uniform_int(rng, chunk[0], chunk[1], npre)
+    gor += pre_g
+    slen += [e + c for e, c in zip(pre_e, pre_c)]
+    ql += pre_c
+    perm = rng.permutation(len(gor))
+    st = Structure(group_parent=None, prefix_len=[prefix] * ng,
+                   group_of_req=[gor[i] for i in perm], suffix_len=[slen[i] for i in perm])
+    p = materialize("chunked", st, dtype=BF16, Hq=32, Hkv=8, d=128, seed=seed,
+                    shuffle_requests=False, poison=poison)
+    q_len = np.asarray([ql[i] for i in perm], np.int32)
+    return p, q_len, chunk_queries(p, q_len)
+
+
 CONFIG_NAMES = ("tiny_fp32", "llama8b", "long_prefix", "skewed", "two_level", "two_level_flat")
 
 
