@@ -51,7 +51,7 @@ DESCRIPTIONS = {
     "tiny_fp32": "2 groups x 8 requests, prefix 256, suffix U[1,64], 4/4 heads, d 64, fp32",
     "chunked": "7 prefill chunks of U[256,512] queries beside 256 decode requests (8 groups x 32, "
                "prefix 2048, suffix U[64,512]), 32/8 heads, d 128, bf16; chunks expanded into "
-               "decode rows with shared 128-token causal levels",
+               "decode rows with shared causal levels (--level-tokens, default 128)",
 }
 
 
@@ -226,7 +226,7 @@ def _make(args, seed=None):
     p, ql, q = W.make_chunked(seed=6 if seed is None else seed, poison=False)
     sh, bt, gor, gpar, plen, slen = chunked.expand(shape_of(p), p.block_table, p.group_of_req,
                                                    p.group_parent, p.prefix_len, p.suffix_len,
-                                                   ql, 128)
+                                                   ql, args.level_tokens)
     p2 = dataclasses.replace(p, q=q, block_table=bt, group_of_req=gor, group_parent=gpar,
                              prefix_len=plen, suffix_len=slen)
     used = sorted(set(int(g) for g in p.group_of_req) - {-1})
@@ -256,6 +256,8 @@ def main():
     ap.add_argument("--workload", default="llama8b", choices=sorted(DESCRIPTIONS))
     ap.add_argument("--groups", type=int, default=None,
                     help="override the number of prefix groups (smaller captures for profiling)")
+    ap.add_argument("--level-tokens", type=int, default=128,
+                    help="causal level size for the chunked workload (multiple of 16)")
     ap.add_argument("--no-baselines", action="store_true",
                     help="skip the CPU-oracle, no-dedup and end-to-end legs")
     args = ap.parse_args()
