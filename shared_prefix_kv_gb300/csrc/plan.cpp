@@ -184,13 +184,15 @@ int build(const Inputs& in, int32_t num_sms, HostPlan& hp) {
   }
   for (int r = 0; r < R; ++r) w_warp += in.slen[r];
 
-  // Chunk targets: a warp item at most half a warp's average share of the
-  // warp work; dense items about three per SM.
+  // Chunk targets: a warp item at most a warp's average share of the warp
+  // work; dense items about one per SM (capped at kDenseMaxChunk tokens).
+  // Measured: more, smaller items cost more in per-item epilogues, tickets
+  // and merges than they gain in balance; the per-warp items fill the gaps.
   const int64_t warps = (int64_t)num_sms * kWarpsPerCta;
-  const int64_t c_warp = std::max<int64_t>(64, round_up(ceil_div(w_warp * Hkv, warps * 2), B));
+  const int64_t c_warp = std::max<int64_t>(64, round_up(ceil_div(w_warp * Hkv, warps), B));
   const int64_t c_dense = std::min<int64_t>(
       kDenseMaxChunk,
-      std::max<int64_t>(256, round_up(ceil_div(w_dense * Hkv, (int64_t)num_sms * 3), kDenseTileTok)));
+      std::max<int64_t>(256, round_up(ceil_div(w_dense * Hkv, (int64_t)num_sms), kDenseTileTok)));
   auto chunking = [&](int64_t len, int64_t target, int32_t* chunk, int32_t* n, int64_t unit) {
     if (len <= 0) { *chunk = (int32_t)B; *n = 0; return; }
     int64_t k = ceil_div(len, target);
