@@ -221,6 +221,15 @@ int64_t psattn_plan_export(psattn_plan_t plan, int32_t which, int32_t* dst, int6
  * queued unit out of range)), or PSATTN_ERR_CUDA. */
 int psattn_plan_status(psattn_plan_t plan, uint32_t* device_flags);
 
+/* Test of the failure path of the kernel's bounded waits, with no fault:
+ * launches one wait on an mbarrier that nothing completes, through the same
+ * bounded wait the decode kernel uses, with a limit of limit_us microseconds
+ * (1 .. 100000).  The wait gives up, the kernel sets error flag 16 and
+ * returns; the context stays usable.  Synchronises the device.  Returns
+ * PSATTN_ERR_DEVICE with *device_flags = 16 when the wait gave up as it
+ * should, PSATTN_OK (flags 0) if it did not, INVALID_ARG or CUDA. */
+int psattn_selftest_wait_timeout(uint32_t limit_us, uint32_t* device_flags);
+
 /* Frees the plan and its workspace (synchronises the device first).  NULL is a no-op. */
 void psattn_plan_destroy(psattn_plan_t plan);
 

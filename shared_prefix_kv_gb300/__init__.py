@@ -45,7 +45,7 @@ EXPORT_WARP_ITEMS, EXPORT_DENSE_ITEMS, EXPORT_REQ, EXPORT_GROUP, EXPORT_MEMBERS,
 
 EXPORTED_SYMBOLS = ("psattn_plan", "psattn_plan_host", "psattn_decode", "psattn_plan_info_get",
                     "psattn_plan_export", "psattn_plan_status", "psattn_plan_destroy",
-                    "psattn_status_string")
+                    "psattn_status_string", "psattn_selftest_wait_timeout")
 
 
 class Shape(ctypes.Structure):
@@ -80,6 +80,8 @@ _lib.psattn_plan_export.argtypes = [_vp, ctypes.c_int32, _vp, ctypes.c_int64]
 _lib.psattn_plan_export.restype = ctypes.c_int64
 _lib.psattn_plan_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint32)]
 _lib.psattn_plan_status.restype = ctypes.c_int
+_lib.psattn_selftest_wait_timeout.argtypes = [ctypes.c_uint32, ctypes.POINTER(ctypes.c_uint32)]
+_lib.psattn_selftest_wait_timeout.restype = ctypes.c_int
 _lib.psattn_plan_destroy.argtypes = [_vp]
 _lib.psattn_plan_destroy.restype = None
 _lib.psattn_status_string.argtypes = [ctypes.c_int]
@@ -167,6 +169,13 @@ def psattn_plan_export(plan: int, which: int) -> np.ndarray:
     buf = np.zeros(max(n, 1), np.int32)
     _lib.psattn_plan_export(plan, which, buf.ctypes.data, n)
     return buf[:n]
+
+
+def psattn_selftest_wait_timeout(limit_us: int):
+    """Returns (status, device_flags) of one kernel wait that nothing completes."""
+    flags = ctypes.c_uint32(0)
+    rc = _lib.psattn_selftest_wait_timeout(int(limit_us), ctypes.byref(flags))
+    return rc, flags.value
 
 
 def psattn_plan_status(plan: int):

@@ -740,17 +740,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // completed and the next one cannot complete before it looks: every wait in
 // this file is placed so that both hold (a stage, buffer or product two phases
 // ahead always depends on something the waiter itself has not yet released).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait_ns(uint32_t bar, uint32_t parity, volatile int* abort,
+                                             uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (global_ns() - t0 > kWaitLimitNs) {
+    if (global_ns() - t0 > limit_ns) {
       *abort = 1;
       return false;
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  return mbar_wait_ns(bar, parity, abort, kWaitLimitNs);
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
@@ -1668,7 +1673,31 @@ int encode_kv_map(CUtensorMap* map, const void* pool, int nblocks, int hkv) {
   return r == CUDA_SUCCESS ? PSATTN_OK : PSATTN_ERR_CUDA;
 }
 
+// One wait that nothing completes (an mbarrier no thread arrives on), run
+// through the same bounded wait as the decode kernel with a short limit: the
+// wait gives up, sets the abort flag and the error word, and the kernel
+// returns.  For testing the bounded-wait path without a fault.
+__global__ void psattn_selftest_wait(uint32_t* flags, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ volatile int abort;
+  if (threadIdx.x == 0) {
+    abort = 0;
+    mbar_init(smem_u32(&bar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const bool ok = mbar_wait_ns(smem_u32(&bar), 0, &abort, limit_ns);
+    if (!ok && abort) atomicOr(flags, (uint32_t)kErrTimeout);
+  }
+}
+
 }  // namespace
+
+int psattn_run_wait_selftest(uint32_t* dev_flags, uint64_t limit_ns, void* stream) {
+  psattn_selftest_wait<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(dev_flags, limit_ns);
+  return cudaGetLastError() == cudaSuccess ? PSATTN_OK : PSATTN_ERR_CUDA;
+}
 
 int psattn_launch_decode(const HostPlan& hp, const DevPlan& dp, const void* q, const void* kv_pool,
                          const int32_t* block_table, const int32_t* group_of_req,

@@ -501,6 +501,25 @@ int psattn_plan_status(psattn_plan_t plan, uint32_t* device_flags) {
   return w ? PSATTN_ERR_DEVICE : PSATTN_OK;
 }
 
+int psattn_selftest_wait_timeout(uint32_t limit_us, uint32_t* device_flags) {
+  if (device_flags) *device_flags = 0;
+  if (limit_us < 1 || limit_us > 100000) return PSATTN_ERR_INVALID_ARG;
+  uint32_t* d = nullptr;
+  uint32_t w = 0;
+  bool ok = cudaMalloc(&d, sizeof w) == cudaSuccess;
+  ok = ok && cudaMemset(d, 0, sizeof w) == cudaSuccess;
+  ok = ok && psattn_run_wait_selftest(d, 1000ull * limit_us, nullptr) == PSATTN_OK;
+  ok = ok && cudaDeviceSynchronize() == cudaSuccess;
+  ok = ok && cudaMemcpy(&w, d, sizeof w, cudaMemcpyDeviceToHost) == cudaSuccess;
+  if (d) cudaFree(d);
+  if (!ok) {
+    cudaGetLastError();
+    return PSATTN_ERR_CUDA;
+  }
+  if (device_flags) *device_flags = w;
+  return w ? PSATTN_ERR_DEVICE : PSATTN_OK;
+}
+
 void psattn_plan_destroy(psattn_plan_t plan) {
   if (!plan) return;
   if (plan->ws) {

@@ -103,6 +103,7 @@ struct DevPlan {
 const psattn::HostPlan* psattn_internal_host_plan(psattn_plan_t plan);
 
 // Implemented in decode.cu.
+int psattn_run_wait_selftest(uint32_t* dev_flags, uint64_t limit_ns, void* stream);
 int psattn_launch_decode(const psattn::HostPlan& hp, const psattn::DevPlan& dp, const void* q,
                          const void* kv_pool, const int32_t* block_table,
                          const int32_t* group_of_req, const int32_t* prefix_len,

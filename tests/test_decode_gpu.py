@@ -194,6 +194,17 @@ def test_suffix_grows_without_replanning():
     _check(p, out, lse)
 
 
+def test_bounded_wait_gives_up_and_reports():
+    """A kernel wait on an mbarrier that nothing completes (1 ms limit) gives
+    up through the decode kernel's own bounded wait: error flag 16 comes back,
+    no fault, and the context still runs a decode with a clean error word."""
+    ps = _lib()
+    rc, flags = ps.psattn_selftest_wait_timeout(1000)
+    assert rc == ps.ERR_DEVICE and flags == 16, (rc, flags)
+    p = W.make("llama8b", small=True)
+    _check(p, *_run(p))
+
+
 def test_device_error_word_on_bad_block_id():
     _lib()
     from workloads.device import DeviceProblem
