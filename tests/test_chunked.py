@@ -47,6 +47,20 @@ def two_level_chunked(seed):
     return p, ql, W.chunk_queries(p, ql)
 
 
+def tiny_fp32_chunked():
+    """The tiny fp32 batch (d 64, GQA 1) with chunks: every third request's
+    whole suffix, and half the suffix of the next ones."""
+    p = W.make("tiny_fp32")
+    ql = np.ones(p.num_req, np.int32)
+    for r in range(0, p.num_req, 3):
+        if p.suffix_len[r] >= 2:
+            ql[r] = int(p.suffix_len[r])
+    for r in range(1, p.num_req, 3):
+        if p.suffix_len[r] >= 4:
+            ql[r] = int(p.suffix_len[r]) // 2
+    return p, ql, W.chunk_queries(p, ql)
+
+
 CASES = [("chunked", s) for s in (6, 7, 8)] + [("two_level", s) for s in (4, 9)]
 
 
@@ -58,6 +72,15 @@ def make_case(kind, seed):
 @pytest.mark.parametrize("kind,seed", CASES)
 def test_expansion_is_exact_under_the_oracle(kind, seed, level_tokens):
     p, ql, q = make_case(kind, seed)
+    p2 = expanded(p, ql, q, level_tokens)
+    o2, l2 = oracle.attention(p2)
+    o1, l1 = oracle.attention_chunked(p, ql, q)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+@pytest.mark.parametrize("level_tokens", [0, 16])
+def test_expansion_is_exact_fp32(level_tokens):
+    p, ql, q = tiny_fp32_chunked()
     p2 = expanded(p, ql, q, level_tokens)
     o2, l2 = oracle.attention(p2)
     o1, l1 = oracle.attention_chunked(p, ql, q)
@@ -154,6 +177,17 @@ def test_gpu_chunked_parity(kind, seed, level_tokens):
     pytest.importorskip("torch")
     p, ql, q = make_case(kind, seed)
     _gpu_check(p, ql, q, level_tokens)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("level_tokens", [0, 16])
+def test_gpu_chunked_fp32_and_simt(level_tokens):
+    """The CUDA-core path (fp32, d 64, GQA 1) under the same expansion: fp32
+    bounds (1e-4)."""
+    pytest.importorskip("torch")
+    p, ql, q = tiny_fp32_chunked()
+    eo, el = _gpu_check(p, ql, q, level_tokens)
+    assert eo <= 1e-4 and el <= 1e-4
 
 
 @pytest.mark.gpu
