@@ -51,7 +51,7 @@ DESCRIPTIONS = {
     "tiny_fp32": "2 groups x 8 requests, prefix 256, suffix U[1,64], 4/4 heads, d 64, fp32",
     "chunked": "7 prefill chunks of U[256,512] queries beside 256 decode requests (8 groups x 32, "
                "prefix 2048, suffix U[64,512]), 32/8 heads, d 128, bf16; chunks expanded into "
-               "decode rows with shared causal levels (--level-tokens, default 128)",
+               "decode rows with shared causal levels (--level-tokens, default 256)",
 }
 
 
@@ -256,7 +256,7 @@ def main():
     ap.add_argument("--workload", default="llama8b", choices=sorted(DESCRIPTIONS))
     ap.add_argument("--groups", type=int, default=None,
                     help="override the number of prefix groups (smaller captures for profiling)")
-    ap.add_argument("--level-tokens", type=int, default=128,
+    ap.add_argument("--level-tokens", type=int, default=256,
                     help="causal level size for the chunked workload (multiple of 16)")
     ap.add_argument("--no-baselines", action="store_true",
                     help="skip the CPU-oracle, no-dedup and end-to-end legs")

@@ -27,7 +27,7 @@ def _p(a):
 
 
 def expand(shape: Shape, block_table, group_of_req, group_parent, prefix_len, suffix_len,
-           q_len, level_tokens: int = 128):
+           q_len, level_tokens: int = 256):
     """Returns (Shape, block_table [R'][maxb], group_of_req [R'], group_parent [G'],
     prefix_len [G'], suffix_len [R']) of the equivalent decode batch."""
     bt, gor, gpar = _i32(block_table), _i32(group_of_req), _i32(group_parent)
