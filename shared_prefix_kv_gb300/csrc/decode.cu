@@ -288,22 +288,29 @@ __device__ __forceinline__ void finish_item(const Params& P, const Item& it, Own
       for (int j = 0; j < ri.n_partials; ++j) {
         if (j == it.slot_j) continue;
         const size_t rix = (((size_t)ri.slot_base + j) * P.Hkv + h) * G + hl;
+        // m, l and O of the partial are loaded together (one round trip); an
+        // empty partial (m = -inf) is skipped after the loads
         const float2 ml = __ldcg(&P.dp.mlpart[rix]);
+        const float* src = P.dp.opart + rix * D;
+        float4 w[NS][SEG / 4];
+#pragma unroll
+        for (int sg = 0; sg < NS; ++sg)
+#pragma unroll
+          for (int e = 0; e < SEG; e += 4)
+            w[sg][e / 4] = __ldcg(reinterpret_cast<const float4*>(src + own.d0[sg] + e));
         if (ml.x == -INFINITY) continue;
         const float Mn = fmaxf(M, ml.x);
         const float a = ex2(M - Mn), b = ex2(ml.x - Mn);
         L = L * a + ml.y * b;
         M = Mn;
-        const float* src = P.dp.opart + rix * D;
 #pragma unroll
         for (int sg = 0; sg < NS; ++sg)
 #pragma unroll
           for (int e = 0; e < SEG; e += 4) {
-            const float4 w = __ldcg(reinterpret_cast<const float4*>(src + own.d0[sg] + e));
-            acc[sg][e] = acc[sg][e] * a + w.x * b;
-            acc[sg][e + 1] = acc[sg][e + 1] * a + w.y * b;
-            acc[sg][e + 2] = acc[sg][e + 2] * a + w.z * b;
-            acc[sg][e + 3] = acc[sg][e + 3] * a + w.w * b;
+            acc[sg][e] = acc[sg][e] * a + w[sg][e / 4].x * b;
+            acc[sg][e + 1] = acc[sg][e + 1] * a + w[sg][e / 4].y * b;
+            acc[sg][e + 2] = acc[sg][e + 2] * a + w[sg][e / 4].z * b;
+            acc[sg][e + 3] = acc[sg][e + 3] * a + w[sg][e / 4].w * b;
           }
       }
       const int hq = h * G + hl;
