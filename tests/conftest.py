@@ -13,7 +13,7 @@ def pytest_configure(config):
 
 
 def pytest_collection_modifyitems(config, items):
-    # GPU tests are never silently skipped on a GPU machine: they fail there if the
+    # GPU tests are never silently skipped on a machine with a GPU: they fail there if the
     # library is missing.  On a machine without a GPU they are skipped.
     try:
         import torch

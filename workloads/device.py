@@ -47,6 +47,6 @@ class DeviceProblem:
 
 
 def tolerances(p):
-    """Bounds from the benchmark spec: max abs error 1e-4 for fp32 inputs, 1e-2 for
+    """Parity bounds: max abs error 1e-4 for fp32 inputs, 1e-2 for
     bf16 inputs (outputs are rounded to bf16), 1e-3 for the LSE."""
     return (1e-4, 1e-4) if p.dtype == W.F32 else (1e-2, 1e-3)
