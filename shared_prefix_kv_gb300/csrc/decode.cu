@@ -196,7 +196,7 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
 }
 
 #ifndef PSATTN_PREFETCH_BLOCKS
-#define PSATTN_PREFETCH_BLOCKS 3
+#define PSATTN_PREFETCH_BLOCKS 2
 #endif
 constexpr int kPrefetchBlocks = PSATTN_PREFETCH_BLOCKS;  // prefetch distance in blocks (0: off)
 static_assert(kPrefetchBlocks >= 0 && kPrefetchBlocks < 32, "prefetch distance");
