@@ -128,7 +128,7 @@ def test_prefix_read_once_per_group(name):
                 if flags:
                     assert not dense
                 else:
-                    assert dense == (nmem * G >= 32)
+                    assert dense == (nmem * G >= 8)
                 want = int(p.prefix_len[g]) * -(-nmem // per_item)
                 for h in range(p.num_kv_heads):
                     assert reads[(g, h)] == want
