@@ -51,7 +51,8 @@ DESCRIPTIONS = {
     "tiny_fp32": "2 groups x 8 requests, prefix 256, suffix U[1,64], 4/4 heads, d 64, fp32",
     "chunked": "7 prefill chunks of U[256,512] queries beside 256 decode requests (8 groups x 32, "
                "prefix 2048, suffix U[64,512]), 32/8 heads, d 128, bf16; chunks expanded into "
-               "decode rows with shared causal levels (--level-tokens, default 256)",
+               "decode rows: each chunk's causal part one ragged level masked per row "
+               "(--chunk-form ragged, default) or levels of --level-tokens",
 }
 
 
@@ -79,10 +80,15 @@ def _peak_bf16():
 
 
 def _visible_tokens(p):
-    """Tokens each row attends to, summed over rows (prefix chain + suffix)."""
+    """Tokens each row attends to, summed over rows (prefix chain + suffix; a
+    ragged leaf level counts its leaf_len tokens)."""
+    leaf = getattr(p, "leaf_len", None)
     total = int(p.suffix_len.sum())
     for r in range(p.num_req):
-        total += sum(int(p.prefix_len[g]) for g in p.chain(r))
+        ch = p.chain(r)
+        total += sum(int(p.prefix_len[g]) for g in ch)
+        if leaf is not None and leaf[r] >= 0 and ch:
+            total -= int(p.prefix_len[ch[-1]]) - int(leaf[r])
     return total
 
 
@@ -224,11 +230,19 @@ def _make(args, seed=None):
     from shared_prefix_kv_gb300 import chunked
     from workloads.device import shape_of
     p, ql, q = W.make_chunked(seed=6 if seed is None else seed, poison=False)
-    sh, bt, gor, gpar, plen, slen = chunked.expand(shape_of(p), p.block_table, p.group_of_req,
-                                                   p.group_parent, p.prefix_len, p.suffix_len,
-                                                   ql, args.level_tokens)
+    if args.chunk_form == "ragged":
+        sh, bt, gor, gpar, plen, slen, leaf = chunked.expand_ragged(
+            shape_of(p), p.block_table, p.group_of_req, p.group_parent, p.prefix_len,
+            p.suffix_len, ql)
+    else:
+        sh, bt, gor, gpar, plen, slen = chunked.expand(shape_of(p), p.block_table,
+                                                       p.group_of_req, p.group_parent,
+                                                       p.prefix_len, p.suffix_len, ql,
+                                                       args.level_tokens)
+        leaf = None
     p2 = dataclasses.replace(p, q=q, block_table=bt, group_of_req=gor, group_parent=gpar,
                              prefix_len=plen, suffix_len=slen)
+    p2.leaf_len = leaf
     used = sorted(set(int(g) for g in p.group_of_req) - {-1})
     tok = sum(int(p.prefix_len[g]) for g in used) + int(p.suffix_len.sum())
     tb = 2 * p.num_kv_heads * p.head_dim * p.elem_bytes
@@ -258,6 +272,8 @@ def main():
                     help="override the number of prefix groups (smaller captures for profiling)")
     ap.add_argument("--level-tokens", type=int, default=256,
                     help="causal level size for the chunked workload (multiple of 16)")
+    ap.add_argument("--chunk-form", choices=["ragged", "levels"], default="ragged",
+                    help="chunked workload: one ragged level per chunk, or fixed-size levels")
     ap.add_argument("--no-baselines", action="store_true",
                     help="skip the CPU-oracle, no-dedup and end-to-end legs")
     args = ap.parse_args()

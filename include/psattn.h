@@ -142,6 +142,28 @@ int psattn_plan_host(const psattn_shape* shape, const int32_t* block_table,
                      int32_t num_sms, psattn_plan_t* out);
 
 /*
+ * psattn_plan / psattn_plan_host with ragged leaf levels: leaf_len (host
+ * int32 [num_req], or NULL for none) gives, per request, how many tokens of
+ * its leaf level (group_of_req[r]) it attends to: the first leaf_len[r]
+ * tokens, or all of them for -1.  The level is still read once for all its
+ * members; each member row masks the tokens past its own length.  This is
+ * how a prefill chunk's causal triangle runs as one shared level
+ * (psattn_chunked.h).  Needs the bf16, head_dim 128 path (else
+ * PSATTN_ERR_UNSUPPORTED).  INVALID_ARG for a length below -1, above the
+ * level, on a request without a group, or with PSATTN_FLATTEN.
+ */
+int psattn_plan_ragged(const psattn_shape* shape, const int32_t* block_table,
+                       const int32_t* group_of_req, const int32_t* group_parent,
+                       const int32_t* prefix_len, const int32_t* suffix_len,
+                       const int32_t* leaf_len, uint32_t flags, psattn_stream_t stream,
+                       psattn_plan_t* out);
+int psattn_plan_host_ragged(const psattn_shape* shape, const int32_t* block_table,
+                            const int32_t* group_of_req, const int32_t* group_parent,
+                            const int32_t* prefix_len, const int32_t* suffix_len,
+                            const int32_t* leaf_len, uint32_t flags, int32_t num_sms,
+                            psattn_plan_t* out);
+
+/*
  * Run one decode step: the whole fused launch (every prefix partial, every
  * suffix partial and the exact LSE merge) as ONE kernel on `stream`.
  * Asynchronous; the plan's counters and tickets reset themselves at the end of

@@ -45,7 +45,8 @@ EXPORT_WARP_ITEMS, EXPORT_DENSE_ITEMS, EXPORT_REQ, EXPORT_GROUP, EXPORT_MEMBERS,
 
 EXPORTED_SYMBOLS = ("psattn_plan", "psattn_plan_host", "psattn_decode", "psattn_plan_info_get",
                     "psattn_plan_export", "psattn_plan_status", "psattn_plan_destroy",
-                    "psattn_status_string", "psattn_selftest_wait_timeout")
+                    "psattn_status_string", "psattn_selftest_wait_timeout",
+                    "psattn_plan_ragged", "psattn_plan_host_ragged")
 
 
 class Shape(ctypes.Structure):
@@ -72,6 +73,12 @@ _lib.psattn_plan.restype = ctypes.c_int
 _lib.psattn_plan_host.argtypes = [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp,
                                   ctypes.c_uint32, ctypes.c_int32, ctypes.POINTER(_vp)]
 _lib.psattn_plan_host.restype = ctypes.c_int
+_lib.psattn_plan_ragged.argtypes = [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp,
+                                    ctypes.c_uint32, _vp, ctypes.POINTER(_vp)]
+_lib.psattn_plan_ragged.restype = ctypes.c_int
+_lib.psattn_plan_host_ragged.argtypes = [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp,
+                                         ctypes.c_uint32, ctypes.c_int32, ctypes.POINTER(_vp)]
+_lib.psattn_plan_host_ragged.restype = ctypes.c_int
 _lib.psattn_decode.argtypes = [_vp] * 9 + [_vp]
 _lib.psattn_decode.restype = ctypes.c_int
 _lib.psattn_plan_info_get.argtypes = [_vp, ctypes.POINTER(PlanInfo)]
@@ -145,6 +152,30 @@ def psattn_plan_host(shape: Shape, block_table, group_of_req, group_parent, pref
     return out.value
 
 
+def psattn_plan_ragged(shape: Shape, block_table, group_of_req, group_parent, prefix_len,
+                       suffix_len, leaf_len, flags: int = 0, stream: int = 0) -> int:
+    arrs = [_i32(block_table), _i32(group_of_req), _i32(group_parent), _i32(prefix_len),
+            _i32(suffix_len), _i32(leaf_len)]
+    out = _vp()
+    rc = _lib.psattn_plan_ragged(ctypes.byref(shape), *[_ptr(a) for a in arrs], flags,
+                                 stream or None, ctypes.byref(out))
+    if rc != OK:
+        raise PsattnError(rc, "psattn_plan_ragged")
+    return out.value
+
+
+def psattn_plan_host_ragged(shape: Shape, block_table, group_of_req, group_parent, prefix_len,
+                            suffix_len, leaf_len, flags: int = 0, num_sms: int = 148) -> int:
+    arrs = [_i32(block_table), _i32(group_of_req), _i32(group_parent), _i32(prefix_len),
+            _i32(suffix_len), _i32(leaf_len)]
+    out = _vp()
+    rc = _lib.psattn_plan_host_ragged(ctypes.byref(shape), *[_ptr(a) for a in arrs], flags,
+                                      int(num_sms), ctypes.byref(out))
+    if rc != OK:
+        raise PsattnError(rc, "psattn_plan_host_ragged")
+    return out.value
+
+
 def psattn_decode(plan: int, q, kv_pool, block_table, group_of_req, prefix_len, suffix_len,
                   out, lse, stream: int = 0) -> None:
     rc = _lib.psattn_decode(plan, _ptr(q), _ptr(kv_pool), _ptr(block_table), _ptr(group_of_req),
@@ -208,8 +239,16 @@ class Plan:
     """Owns a plan handle; ``close()`` (or the context manager) frees it."""
 
     def __init__(self, shape: Shape, block_table, group_of_req, group_parent, prefix_len,
-                 suffix_len, flags: int = 0, stream: int = 0, host_only_sms: Optional[int] = None):
-        if host_only_sms is None:
+                 suffix_len, flags: int = 0, stream: int = 0, host_only_sms: Optional[int] = None,
+                 leaf_len=None):
+        if leaf_len is not None and host_only_sms is None:
+            self.handle = psattn_plan_ragged(shape, block_table, group_of_req, group_parent,
+                                             prefix_len, suffix_len, leaf_len, flags, stream)
+        elif leaf_len is not None:
+            self.handle = psattn_plan_host_ragged(shape, block_table, group_of_req, group_parent,
+                                                  prefix_len, suffix_len, leaf_len, flags,
+                                                  host_only_sms)
+        elif host_only_sms is None:
             self.handle = psattn_plan(shape, block_table, group_of_req, group_parent, prefix_len,
                                       suffix_len, flags, stream)
         else:

@@ -27,16 +27,15 @@ Layout layout_of(int32_t S, int32_t n, int32_t B, int32_t W) {
   return L;
 }
 
-}  // namespace
-
-extern "C" int psattn_chunked_expand(const psattn_shape* shape, const int32_t* block_table,
-                                     const int32_t* group_of_req, const int32_t* group_parent,
-                                     const int32_t* prefix_len, const int32_t* suffix_len,
-                                     const int32_t* q_len, int32_t level_tokens,
-                                     psattn_shape* out_shape, int32_t* out_block_table,
-                                     int32_t* out_group_of_req, int32_t* out_group_parent,
-                                     int32_t* out_prefix_len, int32_t* out_suffix_len,
-                                     int32_t cap_rows, int32_t cap_groups) {
+// ragged: the chunk's causal part is one level whose member i sees its first
+// e_i + 1 tokens (out_leaf_len), instead of level_tokens-sized levels and own
+// suffixes.
+int expand(const psattn_shape* shape, const int32_t* block_table, const int32_t* group_of_req,
+           const int32_t* group_parent, const int32_t* prefix_len, const int32_t* suffix_len,
+           const int32_t* q_len, int32_t level_tokens, bool ragged, psattn_shape* out_shape,
+           int32_t* out_block_table, int32_t* out_group_of_req, int32_t* out_group_parent,
+           int32_t* out_prefix_len, int32_t* out_suffix_len, int32_t* out_leaf_len,
+           int32_t cap_rows, int32_t cap_groups) {
   if (!shape || !out_shape || cap_rows < 0 || cap_groups < 0) return PSATTN_ERR_INVALID_ARG;
   const int32_t R = shape->num_req, NG = shape->num_groups, B = shape->block_size;
   const int32_t maxb = shape->max_blocks_per_req;
@@ -54,16 +53,17 @@ extern "C" int psattn_chunked_expand(const psattn_shape* shape, const int32_t* b
     if (n < 1 || S < 0 || group_of_req[r] < -1 || group_of_req[r] >= NG ||
         (n >= 2 && n > S))
       return PSATTN_ERR_INVALID_ARG;
-    const Layout L = layout_of(S, n, B, level_tokens);
+    const Layout L = layout_of(S, n, B, ragged ? 0 : level_tokens);
     rows += n;
-    groups += (L.A > 0 ? 1 : 0) + L.levels;
+    groups += (L.A > 0 ? 1 : 0) + (ragged ? (n >= 2 ? 1 : 0) : L.levels);
   }
   if (rows > INT32_MAX || groups > INT32_MAX) return PSATTN_ERR_INVALID_ARG;
   *out_shape = *shape;
   out_shape->num_req = (int32_t)rows;
   out_shape->num_groups = (int32_t)groups;
   if (rows > cap_rows || groups > cap_groups) return PSATTN_ERR_NOMEM;
-  if ((rows > 0 && (!out_block_table || !out_group_of_req || !out_suffix_len)) ||
+  if ((rows > 0 && (!out_block_table || !out_group_of_req || !out_suffix_len ||
+                    (ragged && !out_leaf_len))) ||
       (groups > 0 && (!out_group_parent || !out_prefix_len)))
     return PSATTN_ERR_INVALID_ARG;
 
@@ -74,7 +74,7 @@ extern "C" int psattn_chunked_expand(const psattn_shape* shape, const int32_t* b
   int32_t ng = NG;
   int64_t k = 0;
   for (int32_t r = 0; r < R; ++r) {
-    const int32_t n = q_len[r], S = suffix_len[r], W = level_tokens;
+    const int32_t n = q_len[r], S = suffix_len[r], W = ragged ? 0 : level_tokens;
     const int32_t* src = block_table + (size_t)r * maxb;
     const Layout L = layout_of(S, n, B, W);
     int32_t top = group_of_req[r];  // deepest level every query of r shares
@@ -82,6 +82,12 @@ extern "C" int psattn_chunked_expand(const psattn_shape* shape, const int32_t* b
       out_prefix_len[ng] = (int32_t)L.A;
       out_group_parent[ng] = top;
       top = ng++;
+    }
+    int32_t causal = -1;  // the ragged level (ragged mode)
+    if (ragged && n >= 2) {
+      out_prefix_len[ng] = (int32_t)(S - L.A);
+      out_group_parent[ng] = top;
+      causal = ng++;
     }
     const int32_t first_level = ng;
     for (int32_t j = 0; j < L.levels; ++j) {
@@ -91,16 +97,49 @@ extern "C" int psattn_chunked_expand(const psattn_shape* shape, const int32_t* b
     }
     for (int32_t i = 0; i < n; ++i, ++k) {
       std::memcpy(out_block_table + (size_t)k * maxb, src, sizeof(int32_t) * (size_t)maxb);
+      if (ragged) out_leaf_len[k] = -1;
       if (n < 2) {
         out_group_of_req[k] = group_of_req[r];
         out_suffix_len[k] = S;
         continue;
       }
       const int64_t e = L.a - L.A + i;  // position past A, inclusive
+      if (ragged) {
+        out_group_of_req[k] = causal;
+        out_suffix_len[k] = 0;
+        out_leaf_len[k] = (int32_t)(e + 1);
+        continue;
+      }
       const int32_t m = W > 0 ? (int32_t)((e + 1) / W) : 0;
       out_group_of_req[k] = m > 0 ? first_level + m - 1 : top;
       out_suffix_len[k] = (int32_t)(e + 1 - (int64_t)m * (W > 0 ? W : 0));
     }
   }
   return PSATTN_OK;
+}
+
+}  // namespace
+
+extern "C" int psattn_chunked_expand(const psattn_shape* shape, const int32_t* block_table,
+                                     const int32_t* group_of_req, const int32_t* group_parent,
+                                     const int32_t* prefix_len, const int32_t* suffix_len,
+                                     const int32_t* q_len, int32_t level_tokens,
+                                     psattn_shape* out_shape, int32_t* out_block_table,
+                                     int32_t* out_group_of_req, int32_t* out_group_parent,
+                                     int32_t* out_prefix_len, int32_t* out_suffix_len,
+                                     int32_t cap_rows, int32_t cap_groups) {
+  return expand(shape, block_table, group_of_req, group_parent, prefix_len, suffix_len, q_len,
+                level_tokens, false, out_shape, out_block_table, out_group_of_req,
+                out_group_parent, out_prefix_len, out_suffix_len, nullptr, cap_rows, cap_groups);
+}
+
+extern "C" int psattn_chunked_expand_ragged(
+    const psattn_shape* shape, const int32_t* block_table, const int32_t* group_of_req,
+    const int32_t* group_parent, const int32_t* prefix_len, const int32_t* suffix_len,
+    const int32_t* q_len, psattn_shape* out_shape, int32_t* out_block_table,
+    int32_t* out_group_of_req, int32_t* out_group_parent, int32_t* out_prefix_len,
+    int32_t* out_suffix_len, int32_t* out_leaf_len, int32_t cap_rows, int32_t cap_groups) {
+  return expand(shape, block_table, group_of_req, group_parent, prefix_len, suffix_len, q_len, 0,
+                true, out_shape, out_block_table, out_group_of_req, out_group_parent,
+                out_prefix_len, out_suffix_len, out_leaf_len, cap_rows, cap_groups);
 }

@@ -27,6 +27,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <climits>
 #include <cstring>
 
 #include "psattn_internal.h"
@@ -361,9 +362,16 @@ __device__ __forceinline__ void mma_item(const Params& P, const Item& it, int la
   const int nrows = s.nmem * G;
 
   // Q fragments: row g, slice k: chunk (tig + 4*(k>>1)), words 2(k&1) and 2(k&1)+1.
+  // lim: tokens of the span row g attends to (less than the span only on a
+  // ragged leaf level, whose members see its first leaf_vis tokens)
   uint32_t qa0[8], qa2[8];
+  int lim = INT_MAX;
   if (g < nrows) {
     const int r = member_req(P, it, g / G);
+    if (P.dp.any_ragged && it.kind != kItemSuffix) {
+      const ReqInfo ri = P.dp.req[r];
+      if (ri.leaf_vis >= 0 && ri.leaf == it.seg) lim = ri.leaf_vis - s.t0;
+    }
     const __nv_bfloat16* qp =
         reinterpret_cast<const __nv_bfloat16*>(P.q) + ((size_t)r * P.Hq + h * G + g % G) * D;
 #pragma unroll
@@ -441,19 +449,23 @@ __device__ __forceinline__ void mma_item(const Params& P, const Item& it, int la
     // scores of row g for tokens 2tig, 2tig+1, 2tig+8, 2tig+9
     float x[4] = {acc[0][0], acc[0][1], acc[1][0], acc[1][1]};
     float mx = -INFINITY;
+    const int tok0 = bi * kBlockSize;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      x[i] = (tv[i] < nvalid) ? x[i] * P.sl2 : -INFINITY;
+      x[i] = (tv[i] < nvalid && tok0 + tv[i] < lim) ? x[i] * P.sl2 : -INFINITY;
       mx = fmaxf(mx, x[i]);
     }
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const float m_new = fmaxf(m_run, mx);  // finite: the block has a valid token
-    const float alpha = ex2(m_run - m_new);
+    // -inf only for a row that has seen no token yet (padding rows, or a
+    // ragged row past its limit): then O and l are 0 and stay 0
+    const float m_new = fmaxf(m_run, mx);
+    const float mref = (m_new == -INFINITY) ? 0.f : m_new;
+    const float alpha = ex2(m_run - mref);
     float p[4], psum = 0.f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      p[i] = ex2(x[i] - m_new);
+      p[i] = ex2(x[i] - mref);
       psum += p[i];
     }
     l_run = l_run * alpha + psum;
@@ -1150,10 +1162,13 @@ __device__ __noinline__ float softmax_pass_masked(uint32_t sa, float sl2, float 
   return softmax_pass<false>(sa, sl2, m, tile_valid, pa);
 }
 
+// tile_valid may differ between the warp's rows (a ragged leaf level); the
+// pass is chosen for the whole warp (tcgen05.ld is warp-collective)
 __device__ __forceinline__ float softmax_pass_any(uint32_t sa, float sl2, float m, int tile_valid,
                                                   uint32_t pa) {
-  return tile_valid == kTileTok ? softmax_pass_full(sa, sl2, m, pa)
-                                : softmax_pass_masked(sa, sl2, m, tile_valid, pa);
+  return __all_sync(0xffffffffu, tile_valid == kTileTok)
+             ? softmax_pass_full(sa, sl2, m, pa)
+             : softmax_pass_masked(sa, sl2, m, tile_valid, pa);
 }
 
 // Cold path of the softmax: some row's tile sum of P outgrew the limit (its
@@ -1166,7 +1181,8 @@ __device__ __noinline__ bool softmax_regrow(const Params& P, DenseState& d, uint
   // tcgen05.ld is warp-collective: every lane reads the tile max, then selects
   const float tmax = tile_max(sa, P.sl2, tile_valid);
   const float m_new = grow ? tmax : *m_run;
-  const float alpha = ex2(*m_run - m_new);
+  // equal maxima (also a row that has seen no token: both -inf) need no rescale
+  const float alpha = (m_new == *m_run) ? 1.f : ex2(*m_run - m_new);
   *psum = softmax_pass_any(sa, P.sl2, m_new, tile_valid, pa);
   // PV(g - 1) done: pfree of its buffer, completion (g - 1) / 2
   if (!mbar_wait(bar_pfree(d, (g - 1) & 1), ((g - 1) >> 1) & 1, d.abort)) return false;
@@ -1346,21 +1362,26 @@ __device__ void settle_tickets(const Params& P, DenseState& d, MergeRing& ring) 
 // request of this thread's row (-1 past the item's rows).  Returns early
 // (abort set) on a timeout.
 __device__ void softmax_item(const Params& P, DenseState& d, MergeRing& ring, const Item& it,
-                             int ntok, int ntiles, int nrows, int r_row) {
+                             int t0, int ntok, int ntiles, int nrows, int r_row) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t g0 = d.g;
   const uint32_t trow = d.tmem + ((uint32_t)(warp * 32) << 16);
   // the row's partial slots, needed only at the end (the load hides behind the tiles)
-  int sb_row = 0, np_row = 0;
+  // row_end: tokens of the item's span the row attends to (fewer than the
+  // span only on a ragged leaf level, whose members see its first leaf_vis
+  // tokens; 0 when the row sees none of this chunk)
+  int sb_row = 0, np_row = 0, row_end = ntok;
   if (r_row >= 0) {
     const ReqInfo ri = P.dp.req[r_row];
     sb_row = ri.slot_base;
     np_row = ri.n_partials;
+    if (ri.leaf_vis >= 0 && ri.leaf == it.seg) row_end = max(0, min(ntok, ri.leaf_vis - t0));
   }
   float m_run = -INFINITY, l_run = 0.f;
   for (int j = 0; j < ntiles; ++j) {
     const uint32_t g = g0 + j, b = g & 1;
-    const int tile_valid = min(kTileTok, ntok - j * kTileTok);
+    const int tile_valid = min(kTileTok, ntok - j * kTileTok);  // the item's tokens (V rows)
+    const int row_valid = max(0, min(tile_valid, row_end - j * kTileTok));  // this row's
     const uint32_t pa = trow + kTmemP + b * 64;
     if (!mbar_wait(bar_s(d, b), (g >> 1) & 1, d.abort)) return;
     // P buffer b was last read by PV(g - 2)
@@ -1370,11 +1391,11 @@ __device__ void softmax_item(const Params& P, DenseState& d, MergeRing& ring, co
     // P against the running max (the tile's own max on the first tile of the
     // item, when O is still empty); rows whose tile sum outgrew the limit are
     // redone with their new max (rare)
-    if (j == 0) m_run = tile_max(sa, P.sl2, tile_valid);
-    float psum = softmax_pass_any(sa, P.sl2, m_run, tile_valid, pa);
+    if (j == 0) m_run = tile_max(sa, P.sl2, row_valid);
+    float psum = softmax_pass_any(sa, P.sl2, m_run, row_valid, pa);
     const bool grow = psum > kRescaleSumLimit;
     if (j > 0 && __any_sync(0xffffffffu, grow)) {
-      if (!softmax_regrow(P, d, sa, trow, tile_valid, pa, g, grow, &m_run, &l_run, &psum))
+      if (!softmax_regrow(P, d, sa, trow, row_valid, pa, g, grow, &m_run, &l_run, &psum))
         return;
     }
     l_run = (j == 0) ? psum : l_run + psum;
@@ -1531,7 +1552,7 @@ __device__ void dense_loop(const Params& P, uint8_t* smem_raw, MergeRing& ring) 
     int r_row = -1;
     if (tid < 128) r_row = prepare_item(P, d, it, nrows);
     dense_sync();
-    if (tid < 128) softmax_item(P, d, ring, it, ntok, ntiles, nrows, r_row);
+    if (tid < 128) softmax_item(P, d, ring, it, s.t0, ntok, ntiles, nrows, r_row);
     else if (warp == 4) mma_s_item(P, d, ntiles);
     else if (warp == 7) mma_pv_item(P, d, ntiles);
     else if (warp == 5 || warp == 6) producer_item(P, d, s, it.kvh, warp - 5, nb, ntiles);

@@ -42,6 +42,7 @@ struct Inputs {
   const psattn_shape* s;
   const int32_t *bt, *gor, *gpar, *plen, *slen;
   uint32_t flags;
+  const int32_t* leaf_len = nullptr;  // ragged leaf levels (NULL: none)
 };
 
 int check_shape(const psattn_shape* s, uint32_t flags, int32_t* path) {
@@ -128,6 +129,14 @@ int build(const Inputs& in, int32_t num_sms, HostPlan& hp) {
       tokens += in.plen[ch[i]];
       cols += ceil_div(in.plen[ch[i]], B);
       if (flatten && i + 1 < ch.size() && in.plen[ch[i]] % B) return PSATTN_ERR_UNSUPPORTED;
+    }
+    if (in.leaf_len && in.leaf_len[r] != -1) {
+      // a ragged leaf: the request sees the first leaf_len tokens of its leaf
+      // level (the tensor-core and mma.sync paths mask per row)
+      if (leaf < 0 || flatten || in.leaf_len[r] < 0 || in.leaf_len[r] > in.plen[leaf])
+        return PSATTN_ERR_INVALID_ARG;
+      if (path != kPathMmaBf16D128) return PSATTN_ERR_UNSUPPORTED;
+      tokens -= in.plen[leaf] - in.leaf_len[r];
     }
     if (tokens < 1) return PSATTN_ERR_EMPTY_REQUEST;
     if (cols > maxb) return PSATTN_ERR_INVALID_ARG;
@@ -242,6 +251,8 @@ int build(const Inputs& in, int32_t num_sms, HostPlan& hp) {
     ri.slot_base = (int32_t)slot;
     ri.n_partials = j;
     ri.leaf = in.gor[r];
+    ri.leaf_vis = in.leaf_len ? in.leaf_len[r] : -1;
+    if (ri.leaf_vis >= 0) hp.any_ragged = 1;
     slot += j;
     if (slot > INT32_MAX / 2) return PSATTN_ERR_NOMEM;
   }
@@ -322,12 +333,13 @@ namespace {
 
 int plan_common(const psattn_shape* shape, const int32_t* bt, const int32_t* gor,
                 const int32_t* gpar, const int32_t* plen, const int32_t* slen, uint32_t flags,
-                int32_t num_sms, psattn_plan_t* out, std::unique_ptr<psattn_plan_s>& p) {
+                int32_t num_sms, psattn_plan_t* out, std::unique_ptr<psattn_plan_s>& p,
+                const int32_t* leaf_len = nullptr) {
   if (!out) return PSATTN_ERR_INVALID_ARG;
   *out = nullptr;
   p.reset(new (std::nothrow) psattn_plan_s());
   if (!p) return PSATTN_ERR_NOMEM;
-  Inputs in{shape, bt, gor, gpar, plen, slen, flags};
+  Inputs in{shape, bt, gor, gpar, plen, slen, flags, leaf_len};
   try {
     return build(in, num_sms, p->hp);
   } catch (const std::bad_alloc&) {
@@ -373,6 +385,7 @@ int upload(psattn_plan_s* p, cudaStream_t stream) {
   dp.opart = reinterpret_cast<float*>(base + o_op);
   dp.n_witems = (int32_t)hp.witems.size();
   dp.n_ditems = (int32_t)hp.ditems.size();
+  dp.any_ragged = hp.any_ragged;
   cudaError_t e = cudaMemsetAsync(base + o_ctr, 0, o_wi - o_ctr, stream);  // counters + tickets
   auto put = [&](size_t o, const void* src, size_t bytes) {
     if (e == cudaSuccess && bytes) e = cudaMemcpyAsync(base + o, src, bytes, cudaMemcpyHostToDevice, stream);
@@ -408,6 +421,45 @@ int psattn_plan_host(const psattn_shape* shape, const int32_t* block_table,
   int rc = plan_common(shape, block_table, group_of_req, group_parent, prefix_len, suffix_len,
                        flags, num_sms, out, p);
   if (rc) return rc;
+  *out = p.release();
+  return PSATTN_OK;
+}
+
+int psattn_plan_host_ragged(const psattn_shape* shape, const int32_t* block_table,
+                            const int32_t* group_of_req, const int32_t* group_parent,
+                            const int32_t* prefix_len, const int32_t* suffix_len,
+                            const int32_t* leaf_len, uint32_t flags, int32_t num_sms,
+                            psattn_plan_t* out) {
+  std::unique_ptr<psattn_plan_s> p;
+  int rc = plan_common(shape, block_table, group_of_req, group_parent, prefix_len, suffix_len,
+                       flags, num_sms, out, p, leaf_len);
+  if (rc) return rc;
+  *out = p.release();
+  return PSATTN_OK;
+}
+
+int psattn_plan_ragged(const psattn_shape* shape, const int32_t* block_table,
+                       const int32_t* group_of_req, const int32_t* group_parent,
+                       const int32_t* prefix_len, const int32_t* suffix_len,
+                       const int32_t* leaf_len, uint32_t flags, psattn_stream_t stream,
+                       psattn_plan_t* out) {
+  if (!out) return PSATTN_ERR_INVALID_ARG;
+  *out = nullptr;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return PSATTN_ERR_CUDA;
+  }
+  std::unique_ptr<psattn_plan_s> p;
+  int rc = plan_common(shape, block_table, group_of_req, group_parent, prefix_len, suffix_len,
+                       flags, sms, out, p, leaf_len);
+  if (rc) return rc;
+  rc = upload(p.get(), reinterpret_cast<cudaStream_t>(stream));
+  if (rc) {
+    if (p->ws) cudaFree(p->ws);
+    return rc;
+  }
   *out = p.release();
   return PSATTN_OK;
 }

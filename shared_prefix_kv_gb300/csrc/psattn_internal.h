@@ -43,7 +43,8 @@ struct ReqInfo {
   int32_t suffix_chunk;    // tokens per suffix chunk
   int32_t suffix_nchunks;  // suffix chunks (0 when the suffix is empty)
   int32_t leaf;            // leaf group the plan saw (-1 none)
-  int32_t pad0, pad1;
+  int32_t leaf_vis;        // tokens of the leaf level the request attends to (-1: all)
+  int32_t pad1;
 };
 static_assert(sizeof(ReqInfo) == 32, "ReqInfo layout");
 
@@ -80,6 +81,7 @@ struct HostPlan {
   int64_t n_slots = 0;
   int64_t unique_kv_bytes = 0, planned_kv_bytes = 0, qo_bytes = 0;
   int32_t suffix_chunk_max = 0, prefix_chunk_max = 0;
+  int32_t any_ragged = 0;
 };
 
 // Device-side view of a plan's workspace.
@@ -95,6 +97,7 @@ struct DevPlan {
   float* opart;        // [slots][Hkv][G][d] unnormalised partial outputs
   float2* mlpart;      // [slots][Hkv][G] (running max in log2 units, sum)
   int32_t n_witems, n_ditems;
+  int32_t any_ragged;   // some request sees only part of its leaf level
 };
 
 }  // namespace psattn

@@ -218,3 +218,127 @@ def test_gpu_chunked_full_size_sampled():
     assert np.isfinite(out[rows]).all()
     assert np.abs(out[rows] - o_ref).max() <= t_out
     assert np.abs(lse[rows] - l_ref).max() <= t_lse
+
+
+# ------------------------------------------------------------ ragged form
+
+def expanded_ragged(p, q_len, q):
+    sh, bt, gor, gpar, plen, slen, leaf = C.expand_ragged(
+        shape_of(p), p.block_table, p.group_of_req, p.group_parent, p.prefix_len, p.suffix_len,
+        q_len)
+    p2 = dataclasses.replace(p, name=p.name + "_ragged", q=q, block_table=bt, group_of_req=gor,
+                             group_parent=gpar, prefix_len=plen, suffix_len=slen)
+    return p2, leaf
+
+
+def test_ragged_tables():
+    p, ql, q = W.make_chunked(seed=6, small=True)
+    p2, leaf = expanded_ragged(p, ql, q)
+    row = 0
+    for r in range(p.num_req):
+        n = int(ql[r])
+        n_tok = len(oracle.gather_kv(p, r, 0)[0])
+        for i in range(n):
+            assert np.array_equal(p2.block_table[row], p.block_table[r])
+            if n == 1:
+                assert leaf[row] == -1 and p2.suffix_len[row] == p.suffix_len[r]
+            else:
+                g = int(p2.group_of_req[row])
+                assert p2.suffix_len[row] == 0 and 1 <= leaf[row] <= p2.prefix_len[g]
+                # the row sees the chain above its ragged level plus leaf_len tokens
+                chain = p2.chain(row)
+                seen = sum(int(p2.prefix_len[c]) for c in chain[:-1]) + int(leaf[row])
+                assert seen == n_tok - n + i + 1
+            row += 1
+    with ps.Plan(shape_of(p2), p2.block_table, p2.group_of_req, p2.group_parent, p2.prefix_len,
+                 p2.suffix_len, host_only_sms=152, leaf_len=leaf) as pl:
+        assert pl.info()["dense_items"] > 0
+
+
+def test_ragged_plan_reads_the_level_once():
+    from tests.test_plan import tables, item_span
+    p, ql, q = W.make_chunked(seed=7, small=True)
+    p2, leaf = expanded_ragged(p, ql, q)
+    with ps.Plan(shape_of(p2), p2.block_table, p2.group_of_req, p2.group_parent, p2.prefix_len,
+                 p2.suffix_len, host_only_sms=152, leaf_len=leaf) as pl:
+        t = tables(pl)
+        ragged = set(int(p2.group_of_req[k]) for k in range(p2.num_req) if leaf[k] >= 0)
+        G = p.num_q_heads // p.num_kv_heads
+        for g in ragged:
+            members = int((p2.group_of_req == g).sum())
+            per = 4 * (32 // G)
+            for h in range(p.num_kv_heads):
+                tok = sum(item_span(t, it, p2)[1] - item_span(t, it, p2)[0] for it in t["d"]
+                          if it[2] == g and it[1] == h)
+                assert tok == int(p2.prefix_len[g]) * -(-members // per)
+
+
+def test_ragged_invalid():
+    p, ql, q = W.make_chunked(seed=6, small=True)
+    p2, leaf = expanded_ragged(p, ql, q)
+    k = int(np.argmax(leaf))
+    bad = leaf.copy()
+    bad[k] = int(p2.prefix_len[p2.group_of_req[k]]) + 1
+    with pytest.raises(ps.PsattnError):
+        ps.Plan(shape_of(p2), p2.block_table, p2.group_of_req, p2.group_parent, p2.prefix_len,
+                p2.suffix_len, host_only_sms=152, leaf_len=bad)
+    with pytest.raises(ps.PsattnError):  # ragged levels need the bf16 d 128 path
+        ps.Plan(shape_of(p2), p2.block_table, p2.group_of_req, p2.group_parent, p2.prefix_len,
+                p2.suffix_len, flags=ps.SIMT, host_only_sms=152, leaf_len=leaf)
+
+
+def _gpu_check_ragged(p, ql, q, flags=0):
+    from workloads.device import DeviceProblem, tolerances
+    p2, leaf = expanded_ragged(p, ql, q)
+    d = DeviceProblem(p2)
+    with ps.Plan(shape_of(p2), p2.block_table, p2.group_of_req, p2.group_parent, p2.prefix_len,
+                 p2.suffix_len, flags=flags, leaf_len=leaf) as pl:
+        d.decode(pl)
+        out, lse = d.result()
+        rc, dev_flags = pl.status()
+        assert rc == 0 and dev_flags == 0, (rc, dev_flags)
+    o_ref, l_ref = oracle.attention_chunked(p, ql, q)
+    t_out, t_lse = tolerances(p)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+    eo, el = np.abs(out - o_ref).max(), np.abs(lse - l_ref).max()
+    assert eo <= t_out and el <= t_lse, (eo, el)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("flags", ["0", "NO_TENSOR_PREFIX", "NO_DEDUP"])
+@pytest.mark.parametrize("kind,seed", CASES)
+def test_gpu_ragged_parity(kind, seed, flags):
+    """The causal part of each chunk as one ragged level: tensor-core tiles
+    with per-row limits (and, with tensor tiles off or de-duplication off,
+    the mma.sync items with per-row limits)."""
+    pytest.importorskip("torch")
+    p, ql, q = make_case(kind, seed)
+    _gpu_check_ragged(p, ql, q, 0 if flags == "0" else getattr(ps, flags))
+
+
+@pytest.mark.gpu
+def test_gpu_ragged_full_size_sampled():
+    pytest.importorskip("torch")
+    from workloads.device import DeviceProblem, tolerances
+    p, ql, q = W.make_chunked(seed=6)
+    p2, leaf = expanded_ragged(p, ql, q)
+    d = DeviceProblem(p2)
+    with ps.Plan(shape_of(p2), p2.block_table, p2.group_of_req, p2.group_parent, p2.prefix_len,
+                 p2.suffix_len, leaf_len=leaf) as pl:
+        d.decode(pl)
+        out, lse = d.result()
+        rc, dev_flags = pl.status()
+        assert rc == 0 and dev_flags == 0, (rc, dev_flags)
+    starts = np.r_[0, np.cumsum(ql)[:-1]]
+    pre = [r for r in range(p.num_req) if ql[r] > 1]
+    dec = [r for r in range(p.num_req) if ql[r] == 1][::16]
+    sub = sorted(pre + dec)
+    ps_sub = dataclasses.replace(p, block_table=p.block_table[sub],
+                                 group_of_req=p.group_of_req[sub], suffix_len=p.suffix_len[sub])
+    q_sub = np.concatenate([q[starts[r]:starts[r] + ql[r]] for r in sub])
+    o_ref, l_ref = oracle.attention_chunked(ps_sub, ql[sub], q_sub)
+    rows = np.concatenate([np.arange(starts[r], starts[r] + ql[r]) for r in sub])
+    t_out, t_lse = tolerances(p)
+    assert np.isfinite(out[rows]).all()
+    assert np.abs(out[rows] - o_ref).max() <= t_out
+    assert np.abs(lse[rows] - l_ref).max() <= t_lse

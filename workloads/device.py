@@ -32,9 +32,10 @@ class DeviceProblem:
         self.lse = torch.full((p.num_req, p.num_q_heads), float("nan"), device="cuda")
 
     def plan(self, flags=0):
+        # leaf_len: ragged leaf levels, set on problems built by a ragged expansion
         p = self.p
         return ps.Plan(shape_of(p), p.block_table, p.group_of_req, p.group_parent, p.prefix_len,
-                       p.suffix_len, flags=flags)
+                       p.suffix_len, flags=flags, leaf_len=getattr(p, "leaf_len", None))
 
     def decode(self, plan, stream=None):
         s = stream if stream is not None else torch.cuda.current_stream()
