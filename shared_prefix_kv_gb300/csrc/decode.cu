@@ -27,6 +27,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <climits>
 #include <cstring>
 
@@ -1658,12 +1659,18 @@ template <int PATH>
 cudaError_t launch(const Params& P, int grid, cudaStream_t st) {
   const uint32_t smem = (PATH == kPathMmaBf16D128 && P.dp.n_ditems > 0) ? kDenseSmemBytes : 0;
   if (smem) {
-    static bool attr_set = false;  // once per process; the attribute is per function
-    if (!attr_set) {
+    // the attribute is set once per device the process launches on (it holds
+    // for the function on the current device); concurrent first launches on
+    // one device only set it twice
+    constexpr int kMaxDevices = 64;
+    static std::atomic<bool> attr_set[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    if (dev < 0 || dev >= kMaxDevices || !attr_set[dev].load(std::memory_order_acquire)) {
       cudaError_t e = cudaFuncSetAttribute(psattn_fused_decode<PATH>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return e;
-      attr_set = true;
+      if (dev >= 0 && dev < kMaxDevices) attr_set[dev].store(true, std::memory_order_release);
     }
   }
   psattn_fused_decode<PATH><<<grid, kThreads, smem, st>>>(P);
