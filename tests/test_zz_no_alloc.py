@@ -46,6 +46,34 @@ def test_noalloc_matches_decode_two_calls():
             assert np.abs(lse - ref_lse).max() <= t_lse
 
 
+def test_noalloc_ragged_chunked_batch():
+    """A batch with prefill chunks in the ragged form (per-row limits read
+    from the plan's request table) through the no-allocation entry point."""
+    import dataclasses
+
+    import oracle
+    import shared_prefix_kv_gb300 as ps
+    from shared_prefix_kv_gb300 import chunked
+    from workloads.device import DeviceProblem, shape_of, tolerances
+
+    p, ql, q = W.make_chunked(seed=7, small=True)
+    sh, bt, gor, gpar, plen, slen, leaf = chunked.expand_ragged(
+        shape_of(p), p.block_table, p.group_of_req, p.group_parent, p.prefix_len, p.suffix_len, ql)
+    p2 = dataclasses.replace(p, q=q, block_table=bt, group_of_req=gor, group_parent=gpar,
+                             prefix_len=plen, suffix_len=slen)
+    d = DeviceProblem(p2)
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    with ps.Plan(shape_of(p2), bt, gor, gpar, plen, slen, host_only_sms=sms, leaf_len=leaf) as hp:
+        ps.psattn_decode_noalloc(hp.handle, d.q, d.pool, d.bt, d.gor, d.plen, d.slen, d.out,
+                                 d.lse, torch.cuda.current_stream().cuda_stream)
+        out, lse = d.result()
+    o_ref, l_ref = oracle.attention_chunked(p, ql, q)
+    t_out, t_lse = tolerances(p)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+    assert np.abs(out - o_ref).max() <= t_out
+    assert np.abs(lse - l_ref).max() <= t_lse
+
+
 def test_noalloc_rejects_plan_beyond_scratch():
     import shared_prefix_kv_gb300 as ps
 
