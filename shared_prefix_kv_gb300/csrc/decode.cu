@@ -1544,6 +1544,7 @@ __device__ void dense_loop(const Params& P, uint8_t* smem_raw, MergeRing& ring) 
     const Span s = resolve(P, it);
     const int nrows = s.nmem * P.G;
     int ntok = s.t1 - s.t0;
+    if (it.kind == kItemDenseRagged) ntok = min(ntok, it.cost);  // no row sees further
     if (ntok > kMaxDenseBlocks * kBlockSize) {  // device lengths beyond what was planned
       if (control) raise(P, kErrColumn);
       ntok = kMaxDenseBlocks * kBlockSize;

@@ -275,12 +275,27 @@ int build(const Inputs& in, int32_t num_sms, HostPlan& hp) {
     const int per = gi.dense ? mpt : mpi;
     for (int32_t m0 = 0; m0 < gi.n_mem; m0 += per) {
       const int32_t nm = std::min<int32_t>(per, gi.n_mem - m0);
+      // on a ragged level, the farthest token any member of the item sees
+      int64_t reach = 0;
+      bool short_all = gi.dense != 0;
+      for (int32_t m = m0; m < m0 + nm; ++m) {
+        const ReqInfo& ri = hp.req[hp.members[gi.mem_off + m]];
+        const bool ragged = ri.leaf_vis >= 0 && ri.leaf == g;
+        const int64_t lim = ragged ? ri.leaf_vis : level_len(g);
+        if (!ragged) short_all = false;
+        reach = std::max(reach, lim);
+      }
       for (int32_t c = 0; c < gi.n_chunks; ++c) {
-        const int32_t t = seg_tokens(level_len(g), gi.chunk_tok, gi.n_chunks, c);
+        int32_t t = seg_tokens(level_len(g), gi.chunk_tok, gi.n_chunks, c);
+        int32_t kind = gi.dense ? kItemDense : kItemPrefix;
+        if (short_all) {  // tensor-core item on a ragged level: skip the tiles no row sees
+          const int64_t lo = (int64_t)c * gi.chunk_tok;
+          t = (int32_t)std::max<int64_t>(0, std::min<int64_t>(t, reach - lo));
+          kind = kItemDenseRagged;
+        }
         planned_tok += t;
         for (int h = 0; h < Hkv; ++h) {
-          Item it{gi.dense ? kItemDense : kItemPrefix, h, g, c, gi.mem_off + m0, nm,
-                  gi.slot_j0 + c, t};
+          Item it{kind, h, g, c, gi.mem_off + m0, nm, gi.slot_j0 + c, t};
           (gi.dense ? hp.ditems : hp.witems).push_back(it);
         }
       }

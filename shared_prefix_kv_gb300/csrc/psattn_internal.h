@@ -20,7 +20,10 @@ constexpr int kMmaRows = 8;          // q vectors one mma.sync warp item serves 
 constexpr int kSimtRows = 4;         // q vectors one CUDA-core warp item serves
 constexpr int kDenseRows = 128;      // rows of one tensor-core prefix tile (UMMA M)
 
-enum ItemKind : int32_t { kItemSuffix = 0, kItemPrefix = 1, kItemDense = 2 };
+// kItemDenseRagged: a dense item on a ragged level whose members all stop
+// short of the chunk's end; its span ends `cost` tokens past the chunk start
+// (the tiles past every member's limit are skipped).
+enum ItemKind : int32_t { kItemSuffix = 0, kItemPrefix = 1, kItemDense = 2, kItemDenseRagged = 3 };
 
 // Kernel variant chosen at plan time from dtype / head_dim / flags.
 enum Path : int32_t { kPathMmaBf16D128 = 0, kPathSimtF32D64 = 1, kPathSimtF32D128 = 2,

@@ -264,13 +264,19 @@ def test_ragged_plan_reads_the_level_once():
         t = tables(pl)
         ragged = set(int(p2.group_of_req[k]) for k in range(p2.num_req) if leaf[k] >= 0)
         G = p.num_q_heads // p.num_kv_heads
+        per = 4 * (32 // G)
         for g in ragged:
-            members = int((p2.group_of_req == g).sum())
-            per = 4 * (32 // G)
+            # members in row order; a tile of `per` members reads the level up to
+            # the farthest token one of them sees (the rest of the triangle is skipped)
+            lims = [int(leaf[k]) for k in range(p2.num_req) if p2.group_of_req[k] == g]
+            want = sum(min(int(p2.prefix_len[g]), max(lims[i:i + per]))
+                       for i in range(0, len(lims), per))
+            assert want < int(p2.prefix_len[g]) * -(-len(lims) // per)
             for h in range(p.num_kv_heads):
                 tok = sum(item_span(t, it, p2)[1] - item_span(t, it, p2)[0] for it in t["d"]
                           if it[2] == g and it[1] == h)
-                assert tok == int(p2.prefix_len[g]) * -(-members // per)
+                assert tok == want
+                assert all(it[0] == 3 for it in t["d"] if it[2] == g)
 
 
 def test_ragged_invalid():
@@ -342,3 +348,25 @@ def test_gpu_ragged_full_size_sampled():
     assert np.isfinite(out[rows]).all()
     assert np.abs(out[rows] - o_ref).max() <= t_out
     assert np.abs(lse[rows] - l_ref).max() <= t_lse
+
+
+@pytest.mark.gpu
+def test_gpu_ragged_long_chunk_split_into_chunks():
+    """A 300-query chunk that is its request's whole suffix (1200 rows at GQA
+    4) beside a few decode requests: the ragged level is split into chunks, so
+    the tiles of the first queries have a chunk they see nothing of (items of
+    zero tokens that still deliver their empty partials)."""
+    pytest.importorskip("torch")
+    st = W.Structure(group_parent=None, prefix_len=[96], group_of_req=[0, 0, -1, 0],
+                     suffix_len=[300, 40, 33, 9])
+    p = W.materialize("long_chunk", st, dtype=W.BF16, Hq=32, Hkv=8, d=128, seed=3,
+                      shuffle_requests=False)
+    ql = np.array([300, 1, 1, 1], np.int32)
+    q = W.chunk_queries(p, ql)
+    p2, leaf = expanded_ragged(p, ql, q)
+    with ps.Plan(shape_of(p2), p2.block_table, p2.group_of_req, p2.group_parent, p2.prefix_len,
+                 p2.suffix_len, host_only_sms=152, leaf_len=leaf) as pl:
+        from tests.test_plan import tables
+        t = tables(pl)
+        assert (t["d"][:, 0] == 3).any() and (t["d"][:, 7] == 0).any()  # zero-token items
+    _gpu_check_ragged(p, ql, q)

@@ -47,6 +47,8 @@ def item_span(t, it, p):
         ln, ch, n = int(p.prefix_len[seg]) + int(t["add"][seg]), g[1], g[2]
     lo = chunk * ch
     hi = ln if chunk == n - 1 else min(ln, lo + ch)
+    if kind == 3:  # tensor-core item on a ragged level: its span stops at its cost
+        hi = min(hi, lo + int(it[7]))
     return lo, max(lo, hi)
 
 
