@@ -65,15 +65,14 @@ int psattn_chunked_expand(const psattn_shape* shape, const int32_t* block_table,
                           int32_t* out_group_parent, int32_t* out_prefix_len,
                           int32_t* out_suffix_len, int32_t cap_rows, int32_t cap_groups);
 
-/* The same batch with the chunk's causal part as one ragged level, for
- * psattn_plan_ragged (psattn.h): for a request with n >= 2 queries, past the
- * shared level of its earlier suffix comes one level holding the rest of its
- * suffix (the chunk and the partial block before it), shared by all n
- * queries; query i attends to its first out_leaf_len = (position of query i
- * past that level's start) + 1 tokens, and has no suffix of its own.  The
- * tensor-core tile then reads the chunk's K/V once for all n * G query rows
- * and masks each row at its position, the causal attention of the chunk as
- * one masked contraction.  Requests with n = 1 are copied unchanged
+/* The same batch with each chunk's suffix as one ragged level, for
+ * psattn_plan_ragged (psattn.h): for a request with n >= 2 queries, its whole
+ * suffix (the tokens before the chunk and the chunk) becomes one level under
+ * its group, shared by all n queries; query i attends to its first
+ * out_leaf_len = a + i + 1 tokens of it (a = suffix tokens before the chunk),
+ * and has no suffix of its own.  The tensor-core tile then reads the
+ * suffix's K/V once for all n * G query rows and masks each row at its
+ * position: the chunk's causal attention as one masked contraction.  Requests with n = 1 are copied unchanged
  * (out_leaf_len -1).  Arguments and errors as psattn_chunked_expand, plus
  *  out_leaf_len   int32 [cap_rows] out. */
 int psattn_chunked_expand_ragged(const psattn_shape* shape, const int32_t* block_table,

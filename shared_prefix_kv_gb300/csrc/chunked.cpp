@@ -27,9 +27,10 @@ Layout layout_of(int32_t S, int32_t n, int32_t B, int32_t W) {
   return L;
 }
 
-// ragged: the chunk's causal part is one level whose member i sees its first
-// e_i + 1 tokens (out_leaf_len), instead of level_tokens-sized levels and own
-// suffixes.
+// ragged: the request's whole suffix is one level whose member i sees its
+// first a + i + 1 tokens (out_leaf_len; a = suffix tokens before the chunk),
+// instead of a level for the earlier suffix, level_tokens-sized causal levels
+// and own suffixes.
 int expand(const psattn_shape* shape, const int32_t* block_table, const int32_t* group_of_req,
            const int32_t* group_parent, const int32_t* prefix_len, const int32_t* suffix_len,
            const int32_t* q_len, int32_t level_tokens, bool ragged, psattn_shape* out_shape,
@@ -55,7 +56,7 @@ int expand(const psattn_shape* shape, const int32_t* block_table, const int32_t*
       return PSATTN_ERR_INVALID_ARG;
     const Layout L = layout_of(S, n, B, ragged ? 0 : level_tokens);
     rows += n;
-    groups += (L.A > 0 ? 1 : 0) + (ragged ? (n >= 2 ? 1 : 0) : L.levels);
+    groups += ragged ? (n >= 2 ? 1 : 0) : (L.A > 0 ? 1 : 0) + L.levels;
   }
   if (rows > INT32_MAX || groups > INT32_MAX) return PSATTN_ERR_INVALID_ARG;
   *out_shape = *shape;
@@ -78,14 +79,14 @@ int expand(const psattn_shape* shape, const int32_t* block_table, const int32_t*
     const int32_t* src = block_table + (size_t)r * maxb;
     const Layout L = layout_of(S, n, B, W);
     int32_t top = group_of_req[r];  // deepest level every query of r shares
-    if (L.A > 0) {
+    if (!ragged && L.A > 0) {
       out_prefix_len[ng] = (int32_t)L.A;
       out_group_parent[ng] = top;
       top = ng++;
     }
     int32_t causal = -1;  // the ragged level (ragged mode)
     if (ragged && n >= 2) {
-      out_prefix_len[ng] = (int32_t)(S - L.A);
+      out_prefix_len[ng] = S;
       out_group_parent[ng] = top;
       causal = ng++;
     }
@@ -103,13 +104,13 @@ int expand(const psattn_shape* shape, const int32_t* block_table, const int32_t*
         out_suffix_len[k] = S;
         continue;
       }
-      const int64_t e = L.a - L.A + i;  // position past A, inclusive
       if (ragged) {
         out_group_of_req[k] = causal;
         out_suffix_len[k] = 0;
-        out_leaf_len[k] = (int32_t)(e + 1);
+        out_leaf_len[k] = (int32_t)(L.a + i + 1);
         continue;
       }
+      const int64_t e = L.a - L.A + i;  // position past A, inclusive
       const int32_t m = W > 0 ? (int32_t)((e + 1) / W) : 0;
       out_group_of_req[k] = m > 0 ? first_level + m - 1 : top;
       out_suffix_len[k] = (int32_t)(e + 1 - (int64_t)m * (W > 0 ? W : 0));
