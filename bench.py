@@ -51,7 +51,7 @@ DESCRIPTIONS = {
     "tiny_fp32": "2 groups x 8 requests, prefix 256, suffix U[1,64], 4/4 heads, d 64, fp32",
     "chunked": "7 prefill chunks of U[256,512] queries beside 256 decode requests (8 groups x 32, "
                "prefix 2048, suffix U[64,512]), 32/8 heads, d 128, bf16; chunks expanded into "
-               "decode rows: each chunk's causal part one ragged level masked per row "
+               "decode rows: each chunk's suffix one ragged level masked per row "
                "(--chunk-form ragged, default) or levels of --level-tokens",
 }
 
