@@ -46,7 +46,9 @@ DESCRIPTIONS = {
     "skewed": "1024 requests, Zipf(1.2) over 128 groups, 10% ungrouped, prefix LN(1500,0.8) "
               "[64,8192], suffix LN(200,0.7) [1,2048], 32/8 heads, d 128, bf16",
     "two_level": "4096 requests, level-1 prefix 4096 shared by all, level-2 1024 per 64 groups of "
-                 "64, suffix U[32,256], 3-partial merge, 32/8 heads, d 128, bf16",
+                 "64, suffix U[32,256], 32/8 heads, d 128, bf16; the plan folds level 1 into the "
+                 "level-2 groups' tensor-core items (2 partials per request; --no-fold keeps "
+                 "the 3-partial merge), level 1 counted once in the roofline bytes",
     "two_level_flat": "the two-level workload flattened to one 5120-token level per group",
     "tiny_fp32": "2 groups x 8 requests, prefix 256, suffix U[1,64], 4/4 heads, d 64, fp32",
     "chunked": "7 prefill chunks of U[256,512] queries beside 256 decode requests (8 groups x 32, "
@@ -254,6 +256,8 @@ def _config(args, p):
     desc = DESCRIPTIONS.get(args.workload, args.workload)
     if args.groups is not None:
         desc += f" (groups overridden to {args.groups})"
+    if getattr(args, "no_fold", False):
+        desc += " (planned with no folding: every prefix level its own partial)"
     return {"workload": f"{args.workload}: {desc}",
             "requests_per_gpu": p.num_req, "global_batch": p.num_req * args.gpus,
             "parallelism": f"replicas x{args.gpus} (independent batches)",
@@ -274,6 +278,9 @@ def main():
                     help="causal level size for the chunked workload (multiple of 16)")
     ap.add_argument("--chunk-form", choices=["ragged", "levels"], default="ragged",
                     help="chunked workload: one ragged level per chunk, or fixed-size levels")
+    ap.add_argument("--no-fold", action="store_true",
+                    help="plan every prefix level as its own partial (no folding of parent "
+                         "levels into their children's tensor-core items)")
     ap.add_argument("--no-baselines", action="store_true",
                     help="skip the CPU-oracle, no-dedup and end-to-end legs")
     args = ap.parse_args()
@@ -301,7 +308,7 @@ def main():
     alg_override = chunk_info[0] if chunk_info else None
     d = DeviceProblem(p)
     t_plan = time.perf_counter()
-    plan = d.plan()
+    plan = d.plan(ps.NO_FOLD if args.no_fold else 0)
     t_plan = time.perf_counter() - t_plan
     info = plan.info()
     stream = torch.cuda.current_stream()

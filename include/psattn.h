@@ -89,6 +89,11 @@ typedef struct {
                                 number of blocks */
 #define PSATTN_NO_TENSOR_PREFIX 4u /* run dense prefix groups on the per-warp path */
 #define PSATTN_SIMT 8u       /* bf16: use the CUDA-core per-warp path instead of mma.sync */
+#define PSATTN_NO_FOLD 16u   /* keep every level its own partial.  By default a parent level
+                                (a whole number of blocks, no requests of its own) is read
+                                by its children's tensor-core items when they need no more
+                                128-row tiles than the level itself; info.unique_kv_bytes
+                                still counts it once */
 
 typedef struct psattn_plan_s* psattn_plan_t;
 

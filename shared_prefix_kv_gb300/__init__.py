@@ -39,7 +39,7 @@ ERR_NOMEM = -8
 ERR_GROUP_CYCLE = -9
 
 F32, BF16 = 0, 1
-NO_DEDUP, FLATTEN, NO_TENSOR_PREFIX, SIMT = 1, 2, 4, 8
+NO_DEDUP, FLATTEN, NO_TENSOR_PREFIX, SIMT, NO_FOLD = 1, 2, 4, 8, 16
 
 EXPORT_WARP_ITEMS, EXPORT_DENSE_ITEMS, EXPORT_REQ, EXPORT_GROUP, EXPORT_MEMBERS, EXPORT_LEN_ADD = range(6)
 

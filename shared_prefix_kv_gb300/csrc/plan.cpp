@@ -157,14 +157,22 @@ int build(const Inputs& in, int32_t num_sms, HostPlan& hp) {
   auto level_len = [&](int g) -> int64_t { return (int64_t)in.plen[g] + hp.len_add[g]; };
   std::vector<std::vector<int32_t>> mem(NG);
   std::vector<int32_t> col_base(NG, -1);
-  for (int r = 0; r < R; ++r) {
-    int64_t col = 0;
-    for (int32_t g : rchain[r]) {
-      mem[g].push_back(r);
-      col_base[g] = (int32_t)col;  // identical for every member: same chain prefix
-      col += ceil_div(level_len(g), B);
+  auto gather_members = [&]() {
+    for (auto& m : mem) m.clear();
+    col_base.assign(NG, -1);
+    for (int r = 0; r < R; ++r) {
+      int64_t col = 0;
+      for (int32_t g : rchain[r]) {
+        mem[g].push_back(r);
+        col_base[g] = (int32_t)col;  // identical for every member: same chain prefix
+        col += ceil_div(level_len(g), B);
+      }
     }
-  }
+  };
+  gather_members();
+  // levels the roofline counts once each (before any folding below)
+  std::vector<char> level_used(NG, 0);
+  for (int g = 0; g < NG; ++g) level_used[g] = !mem[g].empty();
 
   // ---- dedup check: every member reads the same physical blocks as the first
   if (!no_dedup) {
@@ -179,19 +187,68 @@ int build(const Inputs& in, int32_t num_sms, HostPlan& hp) {
     }
   }
 
-  // ---- dense classification and work estimates (token x KV-head units)
   const int rows_w = (path == kPathMmaBf16D128) ? kMmaRows : kSimtRows;
   const int mpi = no_dedup ? 1 : std::max(1, rows_w / G);  // members per warp prefix item
   const int mpt = kDenseRows / G;                          // members per dense tile
+  // the TMA row coordinate of a block is an int32: (block * 2 + kv) * Hkv * 16
+  const bool tma_ok = (int64_t)s.num_pool_blocks * 2 * Hkv * B <= INT32_MAX;
+  const bool tensor = !no_dedup && !(in.flags & PSATTN_NO_TENSOR_PREFIX) &&
+                      path == kPathMmaBf16D128 && tma_ok;
+
+  // ---- folding parent levels into their children's tensor-core items.
+  // Every 128-row tile of a level reads the whole level.  When all members of
+  // a level sit in child groups that run on tensor-core tiles themselves, and
+  // those children need no more tiles than the level does, each child's tiles
+  // can read the level first and then their own tokens: the same K/V reads
+  // and tile rows, and per member one partial, one item epilogue and one merge
+  // step fewer (the first-level enlargement of BatchLLM section 4.2, applied
+  // where it costs no extra reads).  The level's blocks then lead each child's
+  // span, so it must be a whole number of blocks.
+  if (tensor && !flatten && !(in.flags & PSATTN_NO_FOLD) && !in.leaf_len && in.gpar) {
+    std::vector<int64_t> direct(NG, 0), child_tiles(NG, 0);
+    std::vector<char> small_child(NG, 0), fold(NG, 0);
+    for (int r = 0; r < R; ++r)
+      if (in.gor[r] >= 0) ++direct[in.gor[r]];
+    for (int g = 0; g < NG; ++g) {
+      const int32_t par = in.gpar[g];
+      if (par < 0 || mem[g].empty()) continue;
+      child_tiles[par] += ceil_div((int64_t)mem[g].size(), mpt);
+      if ((int64_t)mem[g].size() * G < kDenseMinRows) small_child[par] = 1;
+    }
+    bool any = false;
+    for (int g = 0; g < NG; ++g) {
+      fold[g] = !mem[g].empty() && in.plen[g] > 0 && in.plen[g] % B == 0 && direct[g] == 0 &&
+                !small_child[g] && child_tiles[g] > 0 &&
+                child_tiles[g] <= ceil_div((int64_t)mem[g].size(), mpt);
+      any = any || fold[g];
+    }
+    if (any) {
+      std::vector<int32_t> kept;
+      for (int r = 0; r < R; ++r) {
+        kept.clear();
+        int32_t pending = 0;  // tokens of folded levels above the next kept one
+        for (int32_t g : rchain[r]) {
+          if (fold[g]) {
+            pending += in.plen[g];
+            continue;
+          }
+          hp.len_add[g] = pending;  // the same for every member: same chain above g
+          pending = 0;
+          kept.push_back(g);
+        }
+        rchain[r] = kept;  // a leaf has direct members, so it is never folded
+      }
+      gather_members();
+    }
+  }
+
+  // ---- dense classification and work estimates (token x KV-head units)
   std::vector<int32_t> dense(NG, 0);
   int64_t w_warp = 0, w_dense = 0;
   for (int g = 0; g < NG; ++g) {
     if (mem[g].empty() || level_len(g) == 0) continue;
     const int64_t rows = (int64_t)mem[g].size() * G;
-    // the TMA row coordinate of a block is an int32: (block * 2 + kv) * Hkv * 16
-    const bool tma_ok = (int64_t)s.num_pool_blocks * 2 * Hkv * B <= INT32_MAX;
-    dense[g] = !no_dedup && !(in.flags & PSATTN_NO_TENSOR_PREFIX) &&
-               path == kPathMmaBf16D128 && rows >= kDenseMinRows && tma_ok;
+    dense[g] = tensor && rows >= kDenseMinRows;
     if (dense[g]) w_dense += ceil_div(mem[g].size(), mpt) * level_len(g);
     else w_warp += ceil_div(mem[g].size(), mpi) * level_len(g);
   }
@@ -323,9 +380,11 @@ int build(const Inputs& in, int32_t num_sms, HostPlan& hp) {
   std::stable_sort(hp.ditems.begin(), hp.ditems.end(), order);
 
   // ---- byte accounting (K+V of all KV heads per token = tb)
+  // (a folded level once, however many children read it; under FLATTEN each
+  // leaf's whole chain, the bytes that mode must read)
   int64_t uniq_tok = 0;
   for (int g = 0; g < NG; ++g)
-    if (!mem[g].empty()) uniq_tok += level_len(g);
+    if (level_used[g]) uniq_tok += flatten ? level_len(g) : in.plen[g];
   for (int r = 0; r < R; ++r) uniq_tok += in.slen[r];
   hp.unique_kv_bytes = uniq_tok * tb;
   hp.planned_kv_bytes = planned_tok * tb;

@@ -158,6 +158,19 @@ def test_edge_three_level_chain():
     _check(p, *_run(p))
 
 
+@pytest.mark.parametrize("case", ["two_children", "chain"])
+@pytest.mark.parametrize("flag", ["default", "NO_FOLD"])
+def test_parity_folded_levels(case, flag):
+    """Parent levels read by their children's tensor-core items (the default
+    plan of these batches) against the oracle, and the same batches with
+    every level its own partial."""
+    ps = _lib()
+    from tests.test_plan import FOLD_CASES, fold_case
+    (groups, parent, members), _, _ = FOLD_CASES[case]
+    p = fold_case(groups, parent, members)
+    _check(p, *_run(p, 0 if flag == "default" else getattr(ps, flag)))
+
+
 def test_edge_empty_batch():
     ps = _lib()
     from workloads.device import shape_of

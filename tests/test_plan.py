@@ -59,16 +59,31 @@ def item_members(t, it):
     return [int(x) for x in t["mem"][mem_off:mem_off + nmem]]
 
 
-def expected_segments(p, flatten=False):
-    """(request -> list of (segment key, length)) from the problem itself."""
+def expected_segments(p, flatten=False, add=None):
+    """(request -> list of (segment key, length)) from the problem itself.
+    add: the plan's len_add table.  A level that leads its children's items
+    (folded) shows there as its length added to the next level down, which
+    then spans both; the walk below takes from each level's add exactly the
+    levels above it, so a wrong add fails the assertion."""
     out = {}
     for r in range(p.num_req):
         ch = p.chain(r)
         segs = []
         if flatten and ch:
             segs.append((("g", ch[-1]), sum(int(p.prefix_len[g]) for g in ch)))
-        else:
+        elif add is None:
             segs += [(("g", g), int(p.prefix_len[g])) for g in ch]
+        else:
+            i = len(ch) - 1
+            while i >= 0:
+                g, need, j = ch[i], int(add[ch[i]]), i - 1
+                while need > 0:
+                    assert j >= 0, "len_add longer than the chain above"
+                    need -= int(p.prefix_len[ch[j]])
+                    j -= 1
+                assert need == 0, "len_add does not end on a level boundary"
+                segs.insert(0, (("g", g), int(p.prefix_len[g]) + int(add[g])))
+                i = j
         segs.append((("s", r), int(p.suffix_len[r])))
         out[r] = [(k, n) for k, n in segs if n > 0]
     return out
@@ -92,7 +107,7 @@ def test_coverage_exact(name, flags):
             for r in item_members(t, it):
                 cover[(r, int(it[1]), key)].append((lo, hi))
                 slots[(r, int(it[1]))].append(int(it[6]))
-        segs = expected_segments(p)
+        segs = expected_segments(p, add=t["add"])
         for r in range(p.num_req):
             nparts = int(t["req"][r][1])
             for h in range(Hkv):
@@ -163,6 +178,75 @@ def test_deterministic_and_sorted():
             assert np.array_equal(ta[k], tb[k])
         cost = ta["w"][:, 7]
         assert (np.diff(cost) <= 0).all()
+
+
+def fold_case(groups, parent, members, Hq=32, Hkv=8, dtype=W.BF16, d=128, seed=0):
+    rng = np.random.default_rng(seed)
+    st = W.Structure(group_parent=parent, prefix_len=groups, group_of_req=members,
+                     suffix_len=[int(x) for x in rng.integers(0, 60, len(members))])
+    return W.materialize("fold", st, dtype=dtype, Hq=Hq, Hkv=Hkv, d=d, seed=seed)
+
+
+FOLD_CASES = {
+    # case: ((prefix_len, group_parent, group_of_req), len_add wanted, folded levels)
+    # parent 256 tokens, two children of 32 members: 2 tiles either way -> folds
+    "two_children": (([256, 100, 37], [-1, 0, 0], [1] * 32 + [2] * 32), {1: 256, 2: 256}, {0}),
+    # root -> mid -> two leaves of 20 members: both upper levels fold
+    "chain": (([128, 64, 50, 0], [-1, 0, 1, 1], [2] * 20 + [3] * 20), {2: 192, 3: 192},
+              {0, 1}),
+    # a request of the parent's own: no fold
+    "direct_member": (([256, 100, 37], [-1, 0, 0], [1] * 32 + [2] * 32 + [0]), {}, set()),
+    # a child of one member (4 rows, no tensor-core tile): no fold
+    "small_child": (([256, 100, 37], [-1, 0, 0], [1] * 32 + [2]), {}, set()),
+    # a parent that ends inside a block: no fold
+    "ragged_parent": (([250, 100, 37], [-1, 0, 0], [1] * 32 + [2] * 32), {}, set()),
+    # three children of 12 members need 3 tiles where the parent needs 2: no fold
+    "more_tiles": (([256, 64, 64, 64], [-1, 0, 0, 0], [1] * 12 + [2] * 12 + [3] * 12), {},
+                   set()),
+}
+
+
+@pytest.mark.parametrize("case", sorted(FOLD_CASES))
+def test_fold_rules(case):
+    (groups, parent, members), want, folded = FOLD_CASES[case]
+    p = fold_case(groups, parent, members)
+    with host_plan(p) as pl, host_plan(p, ps.NO_FOLD) as nf:
+        t, tn = tables(pl), tables(nf)
+        assert {g: int(a) for g, a in enumerate(t["add"]) if a} == want
+        assert not tn["add"].any()
+        # a folded level has no items of its own; its children's items span it
+        segs = {int(it[2]) for it in np.concatenate([t["w"], t["d"]]) if it[0] != 0}
+        assert not (segs & folded)
+        assert folded <= {int(it[2]) for it in tn["d"]}
+        # the roofline counts a folded level once; the tiles read it per child
+        assert pl.info()["unique_kv_bytes"] == nf.info()["unique_kv_bytes"]
+
+
+@pytest.mark.parametrize("flag", ["NO_DEDUP", "NO_TENSOR_PREFIX", "SIMT", "FLATTEN"])
+def test_fold_only_on_tensor_path(flag):
+    (groups, parent, members), _, _ = FOLD_CASES["two_children"]
+    p = fold_case(groups, parent, members)
+    with host_plan(p, getattr(ps, flag)) as pl:
+        t = tables(pl)
+        if flag == "FLATTEN":  # every leaf takes its whole chain instead
+            assert sorted(int(a) for a in t["add"] if a) == [256, 256]
+        else:
+            assert not t["add"].any()
+    q = fold_case(groups, parent, members, dtype=W.F32, d=64, Hq=8, Hkv=2)
+    with host_plan(q) as pl:
+        assert not tables(pl)["add"].any()
+
+
+def test_fold_matches_flatten_on_two_level():
+    """On the two-level workload every first level folds: the default plan
+    runs the same items as FLATTEN and counts the first level once."""
+    p = W.make("two_level")
+    with host_plan(p) as a, host_plan(p, ps.FLATTEN) as f, host_plan(p, ps.NO_FOLD) as n:
+        ta, tf = tables(a), tables(f)
+        for k in ("w", "d", "req", "add"):
+            assert np.array_equal(ta[k], tf[k]), k
+        assert a.info()["unique_kv_bytes"] == n.info()["unique_kv_bytes"]
+        assert a.info()["unique_kv_bytes"] < f.info()["unique_kv_bytes"]
 
 
 def test_flatten_flag_equals_flattened_input():

@@ -69,7 +69,7 @@ def test_random_plan_covers_every_token_once(seed):
                 key = ("s", int(it[2])) if it[0] == 0 else ("g", int(it[2]))
                 for r in item_members(t, it):
                     cover.setdefault((r, int(it[1]), key), []).append((lo, hi))
-            for r, segs in expected_segments(p).items():
+            for r, segs in expected_segments(p, add=t["add"]).items():
                 for h in range(p.num_kv_heads):
                     for key, n in segs:
                         pos = 0
@@ -83,10 +83,30 @@ def test_random_plan_covers_every_token_once(seed):
 @pytest.mark.gpu
 @pytest.mark.parametrize("seed", range(12))
 def test_random_batches_gpu_parity(seed):
+    shapes = [dict(), dict(Hq=16, Hkv=8), dict(dtype=W.F32, d=64, Hq=8, Hkv=2)]
+    _gpu_parity(make_case(1000 + seed, **shapes[seed % 3]))
+
+
+# structures whose default plan folds a parent level into its children's
+# tensor-core items
+FOLDED_SEEDS = [4, 10, 23, 25]
+
+
+def test_folded_seeds_fold():
+    for seed in FOLDED_SEEDS:
+        with host_plan(make_case(seed)) as pl:
+            assert tables(pl)["add"].any(), seed
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("seed", FOLDED_SEEDS)
+def test_random_folded_batches_gpu_parity(seed):
+    _gpu_parity(make_case(seed))
+
+
+def _gpu_parity(p):
     pytest.importorskip("torch")
     from workloads.device import DeviceProblem, tolerances
-    shapes = [dict(), dict(Hq=16, Hkv=8), dict(dtype=W.F32, d=64, Hq=8, Hkv=2)]
-    p = make_case(1000 + seed, **shapes[seed % 3])
     d = DeviceProblem(p)
     with d.plan() as pl:
         d.decode(pl)
