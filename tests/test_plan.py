@@ -393,3 +393,18 @@ def test_abi_exports_every_declared_symbol():
         | set(chunked.EXPORTED_SYMBOLS)
     for name in declared:
         assert hasattr(ps._lib, name), name
+
+
+def test_binding_constants_match_header():
+    """The binding's flags, status codes and dtypes carry the header's values."""
+    text = open(ROOT_HEADER).read()
+    defines = dict(re.findall(r"^#define PSATTN_(\w+)\s+(\d+)u\b", text, flags=re.M))
+    enums = dict(re.findall(r"^\s*PSATTN_(\w+)\s*=\s*(-?\d+)", text, flags=re.M))
+    enums.update(re.findall(r"\bPSATTN_(F32|BF16)\s*=\s*(\d+)", text))
+    flags = {k: int(v) for k, v in defines.items() if k != "NOALLOC_SCRATCH_BYTES"}
+    assert {"NO_DEDUP", "FLATTEN", "NO_TENSOR_PREFIX", "SIMT", "NO_FOLD"} <= set(flags)
+    for k, v in flags.items():
+        assert getattr(ps, k) == v, k
+    assert len(enums) >= 12
+    for k, v in enums.items():
+        assert getattr(ps, k) == int(v), k
