@@ -90,8 +90,9 @@ typedef struct {
 #define PSATTN_NO_TENSOR_PREFIX 4u /* run dense prefix groups on the per-warp path */
 #define PSATTN_SIMT 8u       /* bf16: use the CUDA-core per-warp path instead of mma.sync */
 #define PSATTN_NO_FOLD 16u   /* keep every level its own partial.  By default a parent level
-                                (a whole number of blocks, no requests of its own) is read
-                                by its children's tensor-core items when they need no more
+                                (a whole number of blocks) is read by its children's
+                                tensor-core items when those, plus the tiles of the level's
+                                own requests (none, or at least 8 q rows), need no more
                                 128-row tiles than the level itself; info.unique_kv_bytes
                                 still counts it once */
 

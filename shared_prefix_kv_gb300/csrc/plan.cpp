@@ -196,15 +196,17 @@ int build(const Inputs& in, int32_t num_sms, HostPlan& hp) {
                       path == kPathMmaBf16D128 && tma_ok;
 
   // ---- folding parent levels into their children's tensor-core items.
-  // Every 128-row tile of a level reads the whole level.  When all members of
-  // a level sit in child groups that run on tensor-core tiles themselves, and
-  // those children need no more tiles than the level does, each child's tiles
-  // can read the level first and then their own tokens: the same K/V reads
-  // and tile rows, and per member one partial, one item epilogue and one merge
-  // step fewer (the first-level enlargement of BatchLLM section 4.2, applied
-  // where it costs no extra reads).  The level's blocks then lead each child's
-  // span, so it must be a whole number of blocks.
-  if (tensor && !flatten && !(in.flags & PSATTN_NO_FOLD) && !in.leaf_len && in.gpar) {
+  // Every 128-row tile of a level reads the whole level.  When the members of
+  // a level that sit in child groups run on tensor-core tiles there, and those
+  // children's tiles plus the tiles of the level's own requests are no more
+  // than the level needs anyway, each child's tiles can read the level first
+  // and then their own tokens: the same K/V reads and tile rows, and per
+  // member below the level one partial, one item epilogue and one merge step
+  // fewer (the first-level enlargement of BatchLLM section 4.2, applied where
+  // it costs no extra reads).  The level keeps items for its own requests
+  // only.  Its blocks lead each child's span, so it must be a whole number of
+  // blocks.
+  if (tensor && !flatten && !(in.flags & PSATTN_NO_FOLD) && in.gpar) {
     std::vector<int64_t> direct(NG, 0), child_tiles(NG, 0);
     std::vector<char> small_child(NG, 0), fold(NG, 0);
     for (int r = 0; r < R; ++r)
@@ -217,9 +219,13 @@ int build(const Inputs& in, int32_t num_sms, HostPlan& hp) {
     }
     bool any = false;
     for (int g = 0; g < NG; ++g) {
-      fold[g] = !mem[g].empty() && in.plen[g] > 0 && in.plen[g] % B == 0 && direct[g] == 0 &&
+      // the level's own requests keep tiles of their own, so they too must
+      // fill one (no per-warp item re-reading the level)
+      const bool own_ok = direct[g] == 0 || direct[g] * G >= kDenseMinRows;
+      fold[g] = !mem[g].empty() && in.plen[g] > 0 && in.plen[g] % B == 0 && own_ok &&
                 !small_child[g] && child_tiles[g] > 0 &&
-                child_tiles[g] <= ceil_div((int64_t)mem[g].size(), mpt);
+                child_tiles[g] + ceil_div(direct[g], mpt) <=
+                    ceil_div((int64_t)mem[g].size(), mpt);
       any = any || fold[g];
     }
     if (any) {
@@ -227,8 +233,10 @@ int build(const Inputs& in, int32_t num_sms, HostPlan& hp) {
       for (int r = 0; r < R; ++r) {
         kept.clear();
         int32_t pending = 0;  // tokens of folded levels above the next kept one
-        for (int32_t g : rchain[r]) {
-          if (fold[g]) {
+        const size_t n = rchain[r].size();
+        for (size_t i = 0; i < n; ++i) {
+          const int32_t g = rchain[r][i];
+          if (fold[g] && i + 1 < n) {  // a request's own level stays its own
             pending += in.plen[g];
             continue;
           }
@@ -236,7 +244,7 @@ int build(const Inputs& in, int32_t num_sms, HostPlan& hp) {
           pending = 0;
           kept.push_back(g);
         }
-        rchain[r] = kept;  // a leaf has direct members, so it is never folded
+        rchain[r] = kept;
       }
       gather_members();
     }
@@ -308,7 +316,10 @@ int build(const Inputs& in, int32_t num_sms, HostPlan& hp) {
     ri.slot_base = (int32_t)slot;
     ri.n_partials = j;
     ri.leaf = in.gor[r];
+    // a ragged leaf's visible tokens, counted from the start of its level's
+    // span (which folded levels above it lead)
     ri.leaf_vis = in.leaf_len ? in.leaf_len[r] : -1;
+    if (ri.leaf_vis >= 0) ri.leaf_vis += hp.len_add[ri.leaf];
     if (ri.leaf_vis >= 0) hp.any_ragged = 1;
     slot += j;
     if (slot > INT32_MAX / 2) return PSATTN_ERR_NOMEM;

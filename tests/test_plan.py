@@ -194,8 +194,16 @@ FOLD_CASES = {
     # root -> mid -> two leaves of 20 members: both upper levels fold
     "chain": (([128, 64, 50, 0], [-1, 0, 1, 1], [2] * 20 + [3] * 20), {2: 192, 3: 192},
               {0, 1}),
-    # a request of the parent's own: no fold
+    # one request of the parent's own (4 rows, no tile of its own): no fold
     "direct_member": (([256, 100, 37], [-1, 0, 0], [1] * 32 + [2] * 32 + [0]), {}, set()),
+    # eight requests of the parent's own fill a third tile: 1 + 1 + 1 <= 3 -> folds,
+    # the parent keeps items for those eight
+    "direct_tile": (([256, 100, 37], [-1, 0, 0], [1] * 32 + [2] * 32 + [0] * 8),
+                    {1: 256, 2: 256}, {0}),
+    # children of 30 and 34 members and 40 requests of the parent's own need
+    # 1 + 2 + 2 tiles where the parent alone needs 4: no fold
+    "direct_extra_tile": (([256, 100, 37], [-1, 0, 0], [1] * 30 + [2] * 34 + [0] * 40), {},
+                          set()),
     # a child of one member (4 rows, no tensor-core tile): no fold
     "small_child": (([256, 100, 37], [-1, 0, 0], [1] * 32 + [2]), {}, set()),
     # a parent that ends inside a block: no fold
@@ -214,9 +222,11 @@ def test_fold_rules(case):
         t, tn = tables(pl), tables(nf)
         assert {g: int(a) for g, a in enumerate(t["add"]) if a} == want
         assert not tn["add"].any()
-        # a folded level has no items of its own; its children's items span it
-        segs = {int(it[2]) for it in np.concatenate([t["w"], t["d"]]) if it[0] != 0}
-        assert not (segs & folded)
+        # a folded level keeps items only for its own requests; its children's
+        # items span it
+        for it in np.concatenate([t["w"], t["d"]]):
+            if it[0] != 0 and int(it[2]) in folded:
+                assert all(p.group_of_req[r] == it[2] for r in item_members(t, it))
         assert folded <= {int(it[2]) for it in tn["d"]}
         # the roofline counts a folded level once; the tiles read it per child
         assert pl.info()["unique_kv_bytes"] == nf.info()["unique_kv_bytes"]
