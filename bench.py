@@ -94,13 +94,16 @@ def _visible_tokens(p):
     return total
 
 
-def _traffic_record(workload):
-    """Per-launch DRAM bytes from the committed ncu summary of the Llama-3-8B
-    workload, if it was taken on the current kernel source (else None)."""
-    if workload != "llama8b":
+def _traffic_record(args):
+    """Per-launch DRAM bytes from the committed ncu summary of this workload
+    (profiles/psattn_fused_decode_<workload>.md), if that summary records a
+    full-size launch (a ``dram_bytes_per_launch:`` line) taken on the current
+    kernel source; else None.  The summaries are of the default plan, so any
+    plan or size override gives None."""
+    if args.groups is not None or args.no_fold or args.chunk_form != "ragged":
         return None
     src = os.path.join(ROOT, "shared_prefix_kv_gb300", "csrc", "decode.cu")
-    path = os.path.join(ROOT, "profiles", "psattn_fused_decode_llama8b.md")
+    path = os.path.join(ROOT, "profiles", f"psattn_fused_decode_{args.workload}.md")
     try:
         text = open(path).read()
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
@@ -347,7 +350,7 @@ def main():
     alg_bytes = alg_override or (info["unique_kv_bytes"] + info["qo_bytes"])
     peak, peak_kind = _peak_hbm()
     achieved = alg_bytes / (ms * 1e-3) / 1e9
-    traffic = _traffic_record(args.workload)
+    traffic = _traffic_record(args)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
