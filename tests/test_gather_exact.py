@@ -174,7 +174,7 @@ def test_gather_exact_small(name, flag):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("name", ["llama8b", "long_prefix", "skewed"])
+@pytest.mark.parametrize("name", ["llama8b", "long_prefix", "skewed", "two_level"])
 def test_gather_exact_full_size(name):
     """Every output of the full-size batch, in the benchmark's launch
     configuration."""
@@ -188,16 +188,18 @@ def test_gather_exact_full_size(name):
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("flag", ["0", "NO_TENSOR_PREFIX"])
-@pytest.mark.parametrize("seed", [6, 7])
-def test_gather_exact_chunked_ragged(seed, flag):
+@pytest.mark.parametrize("seed,small", [(6, True), (7, True), (6, False)])
+def test_gather_exact_chunked_ragged(seed, small, flag):
     """Prefill rows in the ragged form: per-row limits on the tensor-core
     tiles (or on the mma.sync items), each row's causal boundary token among
-    the selections."""
+    the selections.  The full-size batch (seed 6, not small) is the
+    benchmark's chunked-prefill batch: 7 chunks of 256-512 queries beside 256
+    decode requests."""
     pytest.importorskip("torch")
     import shared_prefix_kv_gb300 as ps
     from shared_prefix_kv_gb300 import chunked as C
     from workloads.device import DeviceProblem, shape_of
-    p, ql, _ = W.make_chunked(seed=seed, small=True)
+    p, ql, _ = W.make_chunked(seed=seed, small=small)
     q, want, want_lse = one_hot(p, seed=seed, q_len=ql)
     sh, bt, gor, gpar, plen, slen, leaf = C.expand_ragged(
         shape_of(p), p.block_table, p.group_of_req, p.group_parent, p.prefix_len, p.suffix_len, ql)
