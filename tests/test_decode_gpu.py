@@ -158,6 +158,35 @@ def test_edge_three_level_chain():
     _check(p, *_run(p))
 
 
+def long_context_problem():
+    """Long contexts: a 131072-token prefix shared by 8 requests and a
+    65539-token one (not a whole number of blocks) shared by 6, suffixes from
+    0 to 8192 tokens, one ungrouped request with a 100000-token suffix and one
+    with 3.  Llama-3-8B attention shape, bf16; about 1.3 GB of pool."""
+    return _custom(32, 8, 128, W.BF16, groups=[131072, 65539], parent=None,
+                   members=[0] * 8 + [1] * 6 + [-1, -1],
+                   suffix=[8192, 1, 0, 300, 5000, 17, 2048, 64,
+                           7, 4095, 0, 1000, 33, 6000, 100000, 3], seed=12)
+
+
+def test_edge_long_context():
+    """Split-k at its longest: the prefixes run as many tensor-core chunks
+    (or, with tensor tiles off, many per-warp chunks), and the 100000-token
+    suffix as many per-warp chunks.  Each (request, KV head) merges tens of
+    partials.  Checked on every output, with each plan flag that changes the
+    split."""
+    ps = _lib()
+    p = long_context_problem()
+    o_ref, l_ref = oracle.attention(p)
+    from workloads.device import tolerances
+    t_out, t_lse = tolerances(p)
+    for flag in (0, ps.NO_TENSOR_PREFIX, ps.NO_DEDUP):
+        out, lse = _run(p, flag)
+        assert np.isfinite(out).all() and np.isfinite(lse).all()
+        eo, el = np.abs(out - o_ref).max(), np.abs(lse - l_ref).max()
+        assert eo <= t_out and el <= t_lse, (flag, eo, el)
+
+
 @pytest.mark.parametrize("case", ["two_children", "chain"])
 @pytest.mark.parametrize("flag", ["default", "NO_FOLD"])
 def test_parity_folded_levels(case, flag):

@@ -187,6 +187,19 @@ def test_gather_exact_full_size(name):
 
 
 @pytest.mark.gpu
+def test_gather_exact_long_context():
+    """The long-context batch (a 131072-token shared prefix, a 100000-token
+    suffix): every chunk boundary of the long split-k spans."""
+    pytest.importorskip("torch")
+    from tests.test_decode_gpu import long_context_problem
+    p = long_context_problem()
+    q, want, want_lse = one_hot(p, seed=5)
+    p = dataclasses.replace(p, q=q)
+    out, lse = _run_decode(p, 0)
+    _compare(p, out, lse, want, want_lse)
+
+
+@pytest.mark.gpu
 @pytest.mark.parametrize("flag", ["0", "NO_TENSOR_PREFIX"])
 @pytest.mark.parametrize("seed,small", [(6, True), (7, True), (6, False)])
 def test_gather_exact_chunked_ragged(seed, small, flag):
