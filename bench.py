@@ -167,7 +167,19 @@ class ClockSampler:
                 "samples": len(self.samples)}
 
 
-def _oracle_rate(p, budget_s: float, max_req=None):
+def _oracle_threads(world: int) -> int:
+    """Threads for the CPU oracle: the OpenMP default (0) in a single process.
+    Under torchrun every rank gets OMP_NUM_THREADS=1, but the oracle runs on
+    rank 0 alone, so there it takes every core this process may run on."""
+    if world <= 1:
+        return 0
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def _oracle_rate(p, budget_s: float, max_req=None, nthreads: int = 0):
     """Queries/s of the CPU oracle over the first requests of the batch, run in
     blocks until `budget_s` of wall time is spent."""
     import oracle
@@ -176,7 +188,7 @@ def _oracle_rate(p, budget_s: float, max_req=None):
     block = 16
     while done < p.num_req and (max_req is None or done < max_req):
         req = order[done:done + block]
-        oracle.attention(p, req)
+        oracle.attention(p, req, nthreads=nthreads)
         done += len(req)
         if time.perf_counter() - t0 >= budget_s:
             break
@@ -191,15 +203,16 @@ def run_reference(args, p):
     if rank != 0:
         return 0
     import oracle
+    nthreads = _oracle_threads(world)
     # calibrate so that warmup + steps stay within about a minute
-    rate, _, _, cores = _oracle_rate(p, 2.0, max_req=64)
+    rate, _, _, cores = _oracle_rate(p, 2.0, max_req=64, nthreads=nthreads)
     per_step = max(1, min(p.num_req, int(60.0 * rate / max(1, args.steps + args.warmup))))
     rng = np.random.default_rng(0)
     for _ in range(args.warmup):
-        oracle.attention(p, rng.choice(p.num_req, per_step, replace=False))
+        oracle.attention(p, rng.choice(p.num_req, per_step, replace=False), nthreads=nthreads)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.attention(p, rng.choice(p.num_req, per_step, replace=False))
+        oracle.attention(p, rng.choice(p.num_req, per_step, replace=False), nthreads=nthreads)
     dt = time.perf_counter() - t0
     value = per_step * args.steps / dt
     line = {
