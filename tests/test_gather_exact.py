@@ -13,17 +13,22 @@ merged max, so its merge weight e^(m_i - m*) is 0 too.
 So the kernel's bf16 output must equal that V row bit for bit, whatever path
 the plan takes: tensor-core tiles, mma.sync or CUDA-core per-warp items,
 split-k chunks, folded levels, ragged per-row limits, or de-duplication off.
-A wrong block id, slot, KV head, level offset or chunk boundary reads another
-token (or a NaN-poisoned slot) and shows up as a mismatch.  Unlike the
-parity tests, this checks every output of the full-size batches, with no
-sampling and no tolerance.  The fp32 path divides the same fp32 weight out of
-O and l, so its output may differ from V by one rounding (rtol 1e-6).
+Unlike the parity tests, this checks every output of the full-size batches,
+with no sampling and no tolerance.  The parity tests cannot see a single
+dropped or duplicated token in a long context: it moves the output by about
+1/n.  The fp32 path divides the same fp32 weight out of O and l, so its
+output may differ from V by one rounding (rtol 1e-6).
 
-Attention does not depend on the order of the tokens a row reads, so this
-checks the set of tokens each row sees, which is the only thing the order of
-the gather can change.  Among the chosen tokens are each chunk's causal
-boundary (the last token a prefill row sees), each request's first token and
-its last suffix token.
+What it detects: a row whose selected token is not read, or is read twice,
+or is read from the wrong slot, and any read of a NaN-poisoned slot (NaN
+reaches the row's output).  A misread block that no row selected from stays
+invisible, since its tokens score far below the selected one.  So the
+selections aim at the places where indexing goes wrong: besides uniform
+picks, the first and last token of every segment (each prefix level and the
+suffix), and each prefill row's causal boundary (the last token it sees).
+A wrong level offset, block column, slot or chunk boundary shifts those
+tokens in every request and is caught.  Attention does not depend on the
+order of the tokens a row reads, so the set of tokens is what is checked.
 
 The expected rows come from the oracle's gather (pinned against a dense
 scatter in the oracle tests).  The CPU test checks the one-hot construction
@@ -62,15 +67,28 @@ def _code_pool(p, seed):
         k[used] = code[used]
 
 
-def _pick(rng, n_vis):
-    """Token a row selects: often the last visible token (the causal boundary
-    of a prefill row, the last suffix token of a decode row), sometimes the
-    first, otherwise uniform."""
+def _segment_edges(p, r):
+    """Token indices of the first and last token of each segment of request
+    r's token list: its prefix levels, root first, then its suffix."""
+    lens = [int(p.prefix_len[g]) for g in p.chain(r)] + [int(p.suffix_len[r])]
+    edges, start = [], 0
+    for n in lens:
+        if n > 0:
+            edges += [start, start + n - 1]
+        start += n
+    return np.unique(np.asarray(edges, np.int64))
+
+
+def _pick(rng, n_vis, edges):
+    """Token a row selects among its first n_vis tokens: the last visible one
+    (a prefill row's causal boundary, a decode row's last suffix token), a
+    segment edge, or a uniform pick."""
     u = rng.random()
-    if u < 0.25:
+    if u < 0.2:
         return n_vis - 1
-    if u < 0.35:
-        return 0
+    e = edges[edges < n_vis]
+    if u < 0.6 and e.size:
+        return int(e[rng.integers(0, e.size)])
     return int(rng.integers(0, n_vis))
 
 
@@ -89,11 +107,13 @@ def one_hot(p, seed, q_len=None):
     want = np.zeros((rows, Hq, d), np.float64)
     row0 = np.r_[0, np.cumsum(ql)[:-1]]
     for r in range(p.num_req):
+        edges = _segment_edges(p, r)
         for kvh in range(Hkv):
             K, V = oracle.gather_kv(p, r, kvh)
             n = K.shape[0]
+            assert edges[-1] == n - 1
             # selections of every (row, q head) reading this KV head
-            js = np.array([[_pick(rng, n - int(ql[r]) + i + 1) for _ in range(G)]
+            js = np.array([[_pick(rng, n - int(ql[r]) + i + 1, edges) for _ in range(G)]
                            for i in range(int(ql[r]))])
             dots = K @ K[js.ravel()].T  # [n][rows * G]
             dots[js.ravel(), np.arange(js.size)] = -np.inf
@@ -122,20 +142,22 @@ def _compare(p, out, lse, want, want_lse):
 # ---------------------------------------------------------------- CPU
 
 
-@pytest.mark.parametrize("name", ["tiny_fp32", "llama8b", "two_level"])
+@pytest.mark.parametrize("name", ["tiny_fp32", "llama8b", "long_prefix", "skewed", "two_level",
+                                  "two_level_flat"])
 def test_oracle_sees_one_hot(name):
     """The construction's premise, checked with the oracle: attention over the
     coded pool returns the selected V rows and LSE = scale * B * d."""
     p = W.make(name, small=name != "tiny_fp32")
-    q, want, want_lse = one_hot(p, seed=1)
+    q, want, want_lse = one_hot(p, seed=3)  # the inputs of the small GPU cases
     o, l = oracle.attention(dataclasses.replace(p, q=q))
     assert np.abs(o - want).max() <= 1e-12
     assert np.abs(l - want_lse).max() <= 1e-9 * float(want_lse.max())
 
 
-def test_oracle_sees_one_hot_chunked():
-    p, ql, _ = W.make_chunked(seed=6, small=True)
-    q, want, want_lse = one_hot(p, seed=2, q_len=ql)
+@pytest.mark.parametrize("seed", [6, 7])
+def test_oracle_sees_one_hot_chunked(seed):
+    p, ql, _ = W.make_chunked(seed=seed, small=True)
+    q, want, want_lse = one_hot(p, seed=seed, q_len=ql)  # as the small GPU cases
     o, l = oracle.attention_chunked(p, ql, q)
     assert np.abs(o - want).max() <= 1e-12
     assert np.abs(l - want_lse).max() <= 1e-9 * float(want_lse.max())
