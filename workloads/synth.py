@@ -119,6 +119,8 @@ def _fill_normal(out_flat: np.ndarray, dtype: int, seed: int, stream_tag: int) -
     on the number of threads used."""
     n = out_flat.shape[0]
     nchunks = _ceil_div(n, _FILL_CHUNK)
+    if nchunks == 0:
+        return
     children = np.random.SeedSequence([seed, stream_tag]).spawn(nchunks)
 
     def work(i: int) -> None:
@@ -190,7 +192,7 @@ def materialize(name: str, st: Structure, *, dtype: int, Hq: int, Hkv: int, d: i
         cols.extend(int(x) for x in phys[cursor:cursor + nsb])
         cursor += nsb
         rows.append(cols)
-    maxb = max(1, max(len(c) for c in rows))
+    maxb = max(1, max((len(c) for c in rows), default=0))
     bt = np.full((R, maxb), -1, np.int32)
     for r, cols in enumerate(rows):
         bt[r, :len(cols)] = cols
