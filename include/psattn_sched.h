@@ -92,8 +92,11 @@ typedef struct {
  *                 *num_iters = iterations needed) when the run is longer
  *  num_iters      out
  * Errors: PSATTN_ERR_INVALID_ARG for a NULL pointer, negative counts or
- * lengths, decode_len < 1, a group id out of range, n_chunk < 1 or
- * max_requests < 0.  A group with no requests is never admitted. */
+ * lengths, decode_len < 1, a group id out of range, n_chunk < 1,
+ * max_requests < 0, or a batch of more than 2^29 tokens in all (each used
+ * group's prefix once, plus every prompt and output; iterations are counted
+ * in int32).  A group with no requests is never admitted.  The run takes one
+ * simulated iteration per step, at least the longest output's length. */
 int psattn_token_batches(const int32_t* group_prefix, int32_t num_groups,
                          const int32_t* group_of_req, const int32_t* distinct_len,
                          const int32_t* decode_len, int32_t num_req,

@@ -28,6 +28,8 @@ struct Req {
   bool done = false;
 };
 
+constexpr int64_t kMaxTotalTokens = int64_t(1) << 29;
+
 }  // namespace
 
 extern "C" int psattn_token_batches(const int32_t* group_prefix, int32_t num_groups,
@@ -109,6 +111,9 @@ extern "C" int psattn_token_batches(const int32_t* group_prefix, int32_t num_gro
     total += sg[order[k]].prefix;
     for (int32_t r : sg[order[k]].members) total += (int64_t)distinct_len[r] + decode_len[r];
   }
+  // iterations are counted in int32 (the tables and the decode queue's start
+  // iterations): a batch must keep its total tokens below kMaxTotalTokens
+  if (total > kMaxTotalTokens) return PSATTN_ERR_INVALID_ARG;
   const int64_t guard = 2 * total + 2 * (int64_t)NS + 4;
 
   int64_t resident = 0;

@@ -1,7 +1,9 @@
 """Seeded fuzz of the host-side C calls (no GPU): the planner and both
 chunked-prefill expansions, on random valid batches with zero to two values
 corrupted (block ids, group ids, parents, lengths, chunk sizes, pool size,
-table width; extreme values included).
+table width; extreme values included).  Also the grouping calls (prefix
+forest, CHT batches) and the token-batching simulation, with extreme chunk
+sizes, limits and lengths.
 
 Every call must return a status: a crash of the library would end the test
 process.  A batch left intact must expand and plan.  The exceptions are the
@@ -14,6 +16,8 @@ import pytest
 import workloads as W
 import shared_prefix_kv_gb300 as ps
 from shared_prefix_kv_gb300 import chunked as C
+from shared_prefix_kv_gb300 import forest as F
+from shared_prefix_kv_gb300 import sched as S
 
 from tests.test_plan import shape_of
 from tests.test_random_batches import random_structure
@@ -97,3 +101,43 @@ def test_host_calls_return_a_status(block):
                 allowed = flags & ps.FLATTEN or (form == "ragged" and not mma_path) or \
                     (e.status == ps.ERR_UNSUPPORTED and not mma_path and flags & ps.SIMT)
                 assert not clean or allowed, (it, form, e.status, flags)
+
+
+def test_grouping_and_scheduling_calls_return_a_status():
+    ext = [-1, 0, 1, 2, 16, 17, 2 ** 30, 2 ** 31 - 1, -2 ** 31]
+    outcomes = set()
+    for it in range(300):
+        rng = np.random.default_rng([2025, it])
+        roots = [rng.integers(0, 50, size=int(rng.integers(0, 80))).tolist() for _ in range(3)]
+        reqs = [roots[rng.integers(0, 3)][:int(rng.integers(0, 80))] +
+                rng.integers(0, 50, size=int(rng.integers(0, 40))).tolist()
+                for _ in range(int(rng.integers(0, 25)))]
+        chunk = int(rng.choice([16, 8, 1, 32] + ext))
+        try:
+            g = F.forest_group(reqs, chunk=chunk, single=bool(rng.random() < 0.5))
+            outcomes.add("forest ok")
+            assert len(g["group_of_req"]) == len(reqs)
+        except ps.PsattnError as e:
+            assert e.status == ps.ERR_INVALID_ARG and chunk < 1, (it, chunk, e.status)
+        try:
+            F.cht_batches(reqs, chunk=chunk, max_batch=int(rng.choice([1, 4, 64] + ext)),
+                          max_new_chunks=int(rng.choice([0, 1, 5] + ext)))
+            outcomes.add("cht ok")
+        except ps.PsattnError as e:
+            assert e.status == ps.ERR_INVALID_ARG, (it, e.status)
+        R, NG = len(reqs), int(rng.integers(0, 6))
+        gp = rng.integers(0, 300, size=NG)
+        gor = rng.integers(-1, NG, size=R) if NG else -np.ones(R, np.int64)
+        dl, ol = rng.integers(0, 200, size=R), rng.integers(1, 50, size=R)
+        for arr in (gp, gor, dl, ol):
+            if arr.size and rng.random() < 0.3:
+                arr[rng.integers(0, arr.size)] = int(rng.choice(ext))
+        try:
+            S.token_batches(gp, gor, dl, ol, n_chunk=int(rng.choice([64, 512] + ext)),
+                            m_threshold=int(rng.choice([-1, 1000, 100000] + ext)),
+                            max_requests=int(rng.choice([0, 4, 256] + ext)),
+                            reorder=bool(rng.random() < 0.5))
+            outcomes.add("sched ok")
+        except ps.PsattnError as e:
+            assert e.status == ps.ERR_INVALID_ARG, (it, e.status)
+    assert outcomes == {"forest ok", "cht ok", "sched ok"}

@@ -224,3 +224,16 @@ def test_invalid_arguments():
         S.token_batches([1], [0], [1], [1], n_chunk=0)
     with pytest.raises(ps.PsattnError):
         S.token_batches([-1], [0], [1], [1], n_chunk=4)
+
+
+def test_total_tokens_limit():
+    """Iterations are counted in int32, so a batch may hold at most 2^29
+    tokens in all (each used group's prefix once, every prompt and output).
+    One token more is rejected before any simulation; the limit itself runs."""
+    with pytest.raises(ps.PsattnError) as e:
+        S.token_batches([], [-1, -1], [10, 10], [2 ** 30, 3], n_chunk=512)
+    assert e.value.status == ps.ERR_INVALID_ARG
+    with pytest.raises(ps.PsattnError):  # a prefix counts once, but counts
+        S.token_batches([2 ** 29 - 5], [0, 0], [3, 3], [1, 1], n_chunk=512)
+    order, tok, mem = S.token_batches([2 ** 29 - 8], [0, 0], [3, 3], [1, 1], n_chunk=2 ** 28)
+    assert tok[:, 2].sum() == 2 ** 29 - 8 and tok[:, 1].sum() == 6
