@@ -34,7 +34,8 @@
  *            NULL pointer means every group is a root (single level).
  *  prefix_len   int32 [num_groups]: tokens a group's level adds (>= 0).
  *  suffix_len   int32 [R]: the request's own tokens, including the decode
- *            token's K/V (>= 0); a request must attend to >= 1 token.
+ *            token's K/V (>= 0); a request must attend to >= 1 token and to
+ *            at most INT32_MAX tokens (its chain and suffix together).
  *  q, out    [R][Hq][d] in dtype; out is rounded to nearest even for bf16.
  *  lse       float32 [R][Hq], natural log of sum(exp(scaled scores)).
  *

@@ -130,6 +130,9 @@ int build(const Inputs& in, int32_t num_sms, HostPlan& hp) {
       cols += ceil_div(in.plen[ch[i]], B);
       if (flatten && i + 1 < ch.size() && in.plen[ch[i]] % B) return PSATTN_ERR_UNSUPPORTED;
     }
+    // the kernel and the flattened chains count a request's tokens (its whole
+    // chain and suffix, seen or not) in int32
+    if (tokens > INT32_MAX) return PSATTN_ERR_INVALID_ARG;
     if (in.leaf_len && in.leaf_len[r] != -1) {
       // a ragged leaf: the request sees the first leaf_len tokens of its leaf
       // level (the tensor-core and mma.sync paths mask per row)
