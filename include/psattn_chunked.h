@@ -54,9 +54,12 @@ extern "C" {
  *  out_block_table  int32 [cap_rows][max_blocks_per_req]
  *  out_group_of_req, out_suffix_len   int32 [cap_rows]
  *  out_group_parent, out_prefix_len   int32 [cap_groups]
+ * Host memory only: the caller owns every input and output array (a first
+ * call with caps of 0 and NULL outputs returns PSATTN_ERR_NOMEM with the
+ * sizes in out_shape), and the call keeps nothing between calls.
  * Errors: PSATTN_ERR_INVALID_ARG (a NULL pointer, a bad length, group id or
  * q_len, level_tokens not a multiple of block_size), PSATTN_ERR_NOMEM (a cap
- * is too small; out_shape says what is needed). */
+ * is too small; out_shape says what is needed).  Never aborts. */
 int psattn_chunked_expand(const psattn_shape* shape, const int32_t* block_table,
                           const int32_t* group_of_req, const int32_t* group_parent,
                           const int32_t* prefix_len, const int32_t* suffix_len,

@@ -58,7 +58,9 @@
  * tokens, distinct-prompt tokens, common-prefix tokens, requests in the
  * batch (a prefix chunk counts as one), and iter_mem[i] = resident KV tokens
  * at the end of the iteration (before that iteration's finished requests are
- * freed).  Returns a psattn_status (psattn.h); never aborts.
+ * freed).  Returns a psattn_status (psattn.h); never aborts.  Host memory
+ * only: the caller owns every input and output array, and the call keeps
+ * nothing between calls.
  */
 #ifndef PSATTN_SCHED_H_
 #define PSATTN_SCHED_H_
