@@ -94,26 +94,30 @@ def _visible_tokens(p):
     return total
 
 
-def _traffic_record(args):
+def _traffic_record(workload, default_plan=True):
     """Per-launch DRAM bytes from the committed ncu summary of this workload
     (profiles/psattn_fused_decode_<workload>.md), if that summary records a
     full-size launch (a ``dram_bytes_per_launch:`` line) taken on the current
-    kernel source; else None.  The summaries are of the default plan, so any
-    plan or size override gives None."""
-    if args.groups is not None or args.no_fold or args.chunk_form != "ragged":
-        return None
+    kernel source; else None.  Returns (bytes or None, where they come from).
+    The summaries are of the default plan, so any plan or size override gives
+    None.  The bytes are copied from the summary, not measured in this run."""
+    if not default_plan:
+        return None, "none: the committed summaries cover the default plan only"
     src = os.path.join(ROOT, "shared_prefix_kv_gb300", "csrc", "decode.cu")
-    path = os.path.join(ROOT, "profiles", f"psattn_fused_decode_{args.workload}.md")
+    rel = os.path.join("profiles", f"psattn_fused_decode_{workload}.md")
     try:
-        text = open(path).read()
+        text = open(os.path.join(ROOT, rel)).read()
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
         m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
         m_b = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
         if m_sha and m_b and m_sha.group(1) == sha:
-            return int(m_b.group(1))
+            return int(m_b.group(1)), (f"{rel} (ncu dram__bytes_read.sum + dram__bytes_write.sum "
+                                       f"of one full-size launch, same kernel source)")
+        if m_b:
+            return None, f"none: {rel} was taken on another kernel source"
     except OSError:
         pass
-    return None
+    return None, f"none: no summary with full-launch DRAM bytes at {rel}"
 
 
 class ClockSampler:
@@ -123,15 +127,16 @@ class ClockSampler:
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, period_ms: int = 100):
         self.index = index
+        self.period_ms = period_ms
         self.proc = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -235,20 +240,24 @@ def _overrides(args):
 
 
 def _make(args, seed=None):
+    return _make_named(args.workload, seed, _overrides(args), args.chunk_form, args.level_tokens)
+
+
+def _make_named(workload, seed=None, overrides=None, chunk_form="ragged", level_tokens=256):
     """The workload's problem, and (algorithmic KV + q/out bytes, attention
     FLOPs) when the bytes differ from what the plan reports (None otherwise).
     A batch with prefill chunks runs as the library's expansion of it into
     decode rows; its algorithmic bytes count each token of the original batch
     once (a prefix once per group) plus q, out and lse of every query, and its
     FLOPs are 4 * Hq * d per (query, visible token)."""
-    if args.workload != "chunked":
-        return W.make(args.workload, seed=seed, poison=False, **_overrides(args)), None
+    if workload != "chunked":
+        return W.make(workload, seed=seed, poison=False, **(overrides or {})), None
     import dataclasses
     import shared_prefix_kv_gb300 as ps
     from shared_prefix_kv_gb300 import chunked
     from workloads.device import shape_of
     p, ql, q = W.make_chunked(seed=6 if seed is None else seed, poison=False)
-    if args.chunk_form == "ragged":
+    if chunk_form == "ragged":
         sh, bt, gor, gpar, plen, slen, leaf = chunked.expand_ragged(
             shape_of(p), p.block_table, p.group_of_req, p.group_parent, p.prefix_len,
             p.suffix_len, ql)
@@ -256,7 +265,7 @@ def _make(args, seed=None):
         sh, bt, gor, gpar, plen, slen = chunked.expand(shape_of(p), p.block_table,
                                                        p.group_of_req, p.group_parent,
                                                        p.prefix_len, p.suffix_len, ql,
-                                                       args.level_tokens)
+                                                       level_tokens)
         leaf = None
     p2 = dataclasses.replace(p, q=q, block_table=bt, group_of_req=gor, group_parent=gpar,
                              prefix_len=plen, suffix_len=slen)
@@ -281,6 +290,113 @@ def _config(args, p):
             "seed": p.seed}
 
 
+# Every workload of the benchmark's configurations, measured in the default
+# run beside the headline: (label, workload, plan flag names, description).
+PER_WORKLOAD = [
+    ("tiny_fp32", "tiny_fp32", (), None),
+    ("llama8b", "llama8b", (), None),
+    ("long_prefix", "long_prefix", (), None),
+    ("skewed", "skewed", (), None),
+    ("two_level", "two_level", (), None),
+    ("two_level_3partial", "two_level", ("NO_FOLD",),
+     "the two-level workload as a 3-partial merge: level 1, the level-2 group and the "
+     "suffix each their own partial (PSATTN_NO_FOLD)"),
+    ("two_level_flat", "two_level_flat", (), None),
+    ("chunked", "chunked", (), None),
+]
+
+
+def per_workload(torch, ps, local, flush, min_launches=50, min_seconds=0.4, reuse=None):
+    """Each workload of PER_WORKLOAD on this GPU: >= min_launches timed
+    launches (and at least min_seconds of them), L2 flushed before each,
+    CUDA events around each launch on the launching stream, clocks sampled
+    during the timed region; its own roofline against its algorithmic bytes,
+    and the same kernel with de-duplication off.  reuse maps a workload name
+    to an already built (problem, chunk_info) to skip drawing it again."""
+    from workloads.device import DeviceProblem
+    peak, peak_kind = _peak_hbm()
+    stream = torch.cuda.current_stream()
+    out = {}
+    cache = dict(reuse or {})
+
+    def timed(d, pl, n):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+        torch.cuda.synchronize()
+        for a, b in ev:
+            flush.fill_(1)
+            a.record(stream)
+            d.decode(pl, stream)
+            b.record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in ev]
+
+    for label, wl, flag_names, desc in PER_WORKLOAD:
+        if wl not in cache:
+            if wl == "two_level_flat" and "two_level" in cache:
+                # the same requests, pool and tables with every chain collapsed
+                cache = {wl: (W.flatten_problem(cache["two_level"][0]), None)}
+            else:
+                cache = {wl: _make_named(wl)}  # one workload's inputs held at a time
+        p, chunk_info = cache[wl]
+        flags = 0
+        for f in flag_names:
+            flags |= getattr(ps, f)
+        d = DeviceProblem(p)
+        t0 = time.perf_counter()
+        pl = d.plan(flags)
+        plan_ms = 1e3 * (time.perf_counter() - t0)
+        info = pl.info()
+        for _ in range(5):
+            d.decode(pl, stream)
+        est = float(np.mean(timed(d, pl, 5)))
+        n = int(max(min_launches, min(4000, math.ceil(min_seconds * 1e3 / (est + 0.05)))))
+        with ClockSampler(local, period_ms=20) as clk:
+            times = timed(d, pl, n)
+        rc, dflags = pl.status()
+        ms = float(np.mean(times))
+        rows = p.num_req
+        alg = chunk_info[0] if chunk_info else info["unique_kv_bytes"] + info["qo_bytes"]
+        achieved = alg / (ms * 1e-3) / 1e9
+        traffic, traffic_src = _traffic_record(label)
+        e = {"description": desc or DESCRIPTIONS.get(wl, wl),
+             "dtype": "bf16" if p.dtype == W.BF16 else "f32",
+             "launches": n, "ms_per_step": ms, "ms_per_step_median": float(np.median(times)),
+             "value": rows / (ms * 1e-3),
+             "unit": "query rows/s" if chunk_info else UNIT,
+             "rows": rows,
+             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                          "frac": achieved / peak, "algorithmic_bytes_per_launch": alg,
+                          "traffic": traffic, "traffic_source": traffic_src,
+                          "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},
+             "plan_ms": plan_ms, "dense_items": info["dense_items"],
+             "warp_items": info["warp_items"], "partial_slots": info["partial_slots"],
+             "error_word": dflags if rc != 0 else 0,
+             "clocks": clk.summary(),
+             "l2": "flushed (256 MiB write) before every timed launch"}
+        if chunk_info:
+            tf = chunk_info[1] / (ms * 1e-3) / 1e12
+            e["tensor"] = {"flops_per_launch": chunk_info[1], "achieved_tflops": tf,
+                           "peak_tflops": _peak_bf16(), "frac": tf / _peak_bf16()}
+        pl.close()
+        if not flag_names:
+            nd = d.plan(ps.NO_DEDUP)
+            nd_times = timed(d, nd, 20)
+            nd_ms = float(np.mean(nd_times))
+            nd_info = nd.info()
+            e["no_dedup"] = {
+                "ms_per_step": nd_ms, "value": rows / (nd_ms * 1e-3), "launches": 20,
+                "gbs_own_bytes": (nd_info["planned_kv_bytes"] + nd_info["qo_bytes"])
+                / (nd_ms * 1e-3) / 1e9,
+                "gbs_dedup_bytes": alg / (nd_ms * 1e-3) / 1e9,
+                "speedup_of_dedup": nd_ms / ms}
+            nd.close()
+        out[label] = e
+        del d
+        torch.cuda.empty_cache()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -299,6 +415,9 @@ def main():
                          "levels into their children's tensor-core items)")
     ap.add_argument("--no-baselines", action="store_true",
                     help="skip the CPU-oracle, no-dedup and end-to-end legs")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="skip the per_workload block (every configuration's own "
+                         "measurement, single-GPU runs only)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     rank, world, local = _dist_env()
@@ -363,7 +482,8 @@ def main():
     alg_bytes = alg_override or (info["unique_kv_bytes"] + info["qo_bytes"])
     peak, peak_kind = _peak_hbm()
     achieved = alg_bytes / (ms * 1e-3) / 1e9
-    traffic = _traffic_record(args)
+    traffic, traffic_src = _traffic_record(
+        args.workload, args.groups is None and not args.no_fold and args.chunk_form == "ragged")
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -373,6 +493,7 @@ def main():
         "config": _config(args, p),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
+                     "traffic_source": traffic_src,
                      "kernel": "psattn_fused_decode",
                      "algorithmic_bytes_per_launch": alg_bytes,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
@@ -479,6 +600,13 @@ def main():
                                               f"wall, all heads, double precision)"}
 
     plan.close()
+    if world == 1 and not args.no_per_workload:
+        del d
+        torch.cuda.empty_cache()
+        reuse = {args.workload: (p, chunk_info)} if args.groups is None and \
+            args.chunk_form == "ragged" and args.workload in dict(
+                (w, 1) for _, w, _, _ in PER_WORKLOAD) else None
+        line["per_workload"] = per_workload(torch, ps, local, flush, reuse=reuse)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:

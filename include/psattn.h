@@ -212,10 +212,13 @@ int psattn_decode(psattn_plan_t plan, const void* q, const void* kv_pool,
  *  other arguments: as psattn_decode (device pointers, same layouts).
  *
  * The first call on a device looks up the array's device address with that
- * device current; make that first call before any stream capture.  Every call
- * clears the counters and tickets and uploads its plan's tables into the
- * array, then runs the same fused kernel as psattn_decode, asynchronously on
- * `stream`.  All calls share the array: calls whose launches overlap on the
+ * device current; make that first call before any stream capture.  The address
+ * is kept per device and looked up again when the device's context has been
+ * replaced (after cudaDeviceReset, for instance).  Every call clears the
+ * counters and tickets and uploads its plan's tables into the array with
+ * asynchronous copies from the plan's host memory, then runs the same fused
+ * kernel as psattn_decode, asynchronously on `stream`: keep the plan alive
+ * until that work on `stream` has completed.  All calls share the array: calls whose launches overlap on the
  * GPU race and give wrong results.  The kernel's error word is kept in the
  * array and is not reported.  Returns INVALID_ARG (null or misaligned pointer),
  * NOMEM (the plan's workspace exceeds PSATTN_NOALLOC_SCRATCH_BYTES; nothing is
@@ -241,7 +244,12 @@ int psattn_plan_info_get(psattn_plan_t plan, psattn_plan_info* info);
  * number of int32 values the table holds, or a negative status. */
 int64_t psattn_plan_export(psattn_plan_t plan, int32_t which, int32_t* dst, int64_t cap);
 
-/* Synchronises the device, reads and clears the kernel's error word.  Returns
+/* Waits for the plan's last psattn_decode launch (an event the library
+ * records after each launch; other work on the device is not waited for),
+ * then reads and clears the kernel's error word.  When the word is non-zero,
+ * the plan's work counters and merge tickets are reset too: a launch that
+ * gave up part way may leave tickets short of their count, and the next
+ * launch must not merge partials left from it.  Returns
  * PSATTN_OK, PSATTN_ERR_DEVICE (flags in *device_flags when non-NULL: 1 =
  * block id out of range, 2 = group_of_req differs from the plan, 4 = block
  * column beyond the table, 8 = a request with no token, 16 = a bounded wait
@@ -259,7 +267,8 @@ int psattn_plan_status(psattn_plan_t plan, uint32_t* device_flags);
  * should, PSATTN_OK (flags 0) if it did not, INVALID_ARG or CUDA. */
 int psattn_selftest_wait_timeout(uint32_t limit_us, uint32_t* device_flags);
 
-/* Frees the plan and its workspace (synchronises the device first).  NULL is a no-op. */
+/* Frees the plan and its workspace, after waiting for the plan's last launch.
+ * NULL is a no-op. */
 void psattn_plan_destroy(psattn_plan_t plan);
 
 /* Static text for a status code. */

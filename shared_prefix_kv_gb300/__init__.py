@@ -46,7 +46,7 @@ EXPORT_WARP_ITEMS, EXPORT_DENSE_ITEMS, EXPORT_REQ, EXPORT_GROUP, EXPORT_MEMBERS,
 EXPORTED_SYMBOLS = ("psattn_plan", "psattn_plan_host", "psattn_decode", "psattn_plan_info_get",
                     "psattn_plan_export", "psattn_plan_status", "psattn_plan_destroy",
                     "psattn_status_string", "psattn_selftest_wait_timeout",
-                    "psattn_plan_ragged", "psattn_plan_host_ragged")
+                    "psattn_plan_ragged", "psattn_plan_host_ragged", "psattn_decode_noalloc")
 
 
 class Shape(ctypes.Structure):

@@ -17,7 +17,11 @@
 //    process exits.
 //  * The first call on a device looks up the array's device address
 //    (cudaGetSymbolAddress) with that device current; make that first call
-//    before any stream capture.  Later calls reuse the cached address.
+//    before any stream capture.  Later calls reuse the cached address while
+//    the device's context stays the same one (its driver context id); after
+//    a cudaDeviceReset the address is looked up again.
+//  * The plan's tables reach the array by asynchronous copies from the
+//    plan's host memory: the plan must outlive the call's work on its stream.
 //  * All calls share the one array and it keeps the last call's contents: each
 //    call clears the counters and tickets, then uploads its plan's tables.
 //    Calls whose launches overlap on the GPU (different streams, or different
@@ -26,6 +30,7 @@
 //    device work.  The kernel's error word also lives in the array and is not
 //    reported (psattn_plan_status reads only a plan's own workspace).
 // No cudaMalloc, cudaFree or other allocating call is made here.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -43,8 +48,40 @@ __device__ __align__(256) unsigned char g_scratch[PSATTN_NOALLOC_SCRATCH_BYTES];
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};  // context id the address belongs to
 
-// Device address of g_scratch on the current device, looked up once per device.
+// Unique id of the calling thread's current driver context (ids are never
+// reused within a process); false when there is none or the driver lacks
+// the calls, and then the address is looked up on every call.
+bool current_context_id(unsigned long long* id) {
+  using GetCurrentFn = CUresult (*)(CUcontext*);
+  using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    void* a = nullptr;
+    void* b = nullptr;
+    cudaDriverEntryPointQueryResult qa, qb;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) ==
+            cudaSuccess &&
+        qa == cudaDriverEntryPointSuccess &&
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) ==
+            cudaSuccess &&
+        qb == cudaDriverEntryPointSuccess) {
+      get_current = reinterpret_cast<GetCurrentFn>(a);
+      get_id = reinterpret_cast<GetIdFn>(b);
+    }
+    cudaGetLastError();
+    tried = true;
+  }
+  if (!get_current || !get_id) return false;
+  CUcontext ctx = nullptr;
+  return get_current(&ctx) == CUDA_SUCCESS && ctx && get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of g_scratch on the current device: looked up with the
+// device current, and again whenever the device's context has changed.
 int scratch_address(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -52,14 +89,19 @@ int scratch_address(void** out) {
     return PSATTN_ERR_CUDA;
   }
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_addr[dev]) {
+  unsigned long long ctx = 0;
+  bool have_ctx = current_context_id(&ctx);
+  if (!g_scratch_addr[dev] || !have_ctx || ctx != g_scratch_ctx[dev]) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
     if (e != cudaSuccess || !p) {
       cudaGetLastError();
       return PSATTN_ERR_CUDA;
     }
+    // the lookup makes the device's primary context current if none was
+    if (!have_ctx) have_ctx = current_context_id(&ctx);
     g_scratch_addr[dev] = p;
+    g_scratch_ctx[dev] = have_ctx ? ctx : 0;
   }
   *out = g_scratch_addr[dev];
   return PSATTN_OK;

@@ -414,6 +414,9 @@ struct psattn_plan_s {
   bool on_device = false;
   void* ws = nullptr;
   size_t ws_bytes = 0;
+  size_t reset_bytes = 0;        // counters + tickets at the head of ws
+  cudaEvent_t done = nullptr;    // recorded after every launch on this plan
+  cudaStream_t aux = nullptr;    // the plan's own stream for status reads and resets
   DevPlan dp{};
 };
 
@@ -454,6 +457,12 @@ int upload(psattn_plan_s* p, cudaStream_t stream) {
   const size_t o_ml = take(sizeof(float2) * (size_t)hp.n_slots * Hkv * G);
   const size_t o_op = take(sizeof(float) * (size_t)hp.n_slots * Hkv * G * d);
   p->ws_bytes = off;
+  p->reset_bytes = o_wi - o_ctr;
+  if (cudaEventCreateWithFlags(&p->done, cudaEventDisableTiming) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&p->aux, cudaStreamNonBlocking) != cudaSuccess) {
+    cudaGetLastError();
+    return PSATTN_ERR_CUDA;
+  }
   if (cudaMalloc(&p->ws, off) != cudaSuccess) {
     cudaGetLastError();
     p->ws = nullptr;
@@ -491,6 +500,18 @@ int upload(psattn_plan_s* p, cudaStream_t stream) {
   }
   p->on_device = true;
   return PSATTN_OK;
+}
+
+// Releases what upload() created (any part of it may be missing).
+void release_device(psattn_plan_s* p) {
+  if (p->done) cudaEventSynchronize(p->done);
+  if (p->ws) cudaFree(p->ws);
+  if (p->done) cudaEventDestroy(p->done);
+  if (p->aux) cudaStreamDestroy(p->aux);
+  cudaGetLastError();
+  p->ws = nullptr;
+  p->done = nullptr;
+  p->aux = nullptr;
 }
 
 }  // namespace
@@ -545,7 +566,7 @@ int psattn_plan_ragged(const psattn_shape* shape, const int32_t* block_table,
   if (rc) return rc;
   rc = upload(p.get(), reinterpret_cast<cudaStream_t>(stream));
   if (rc) {
-    if (p->ws) cudaFree(p->ws);
+    release_device(p.get());
     return rc;
   }
   *out = p.release();
@@ -570,7 +591,7 @@ int psattn_plan(const psattn_shape* shape, const int32_t* block_table,
   if (rc) return rc;
   rc = upload(p.get(), reinterpret_cast<cudaStream_t>(stream));
   if (rc) {
-    if (p->ws) cudaFree(p->ws);
+    release_device(p.get());
     return rc;
   }
   *out = p.release();
@@ -591,8 +612,15 @@ int psattn_decode(psattn_plan_t plan, const void* q, const void* kv_pool,
   if (misaligned(q) || misaligned(kv_pool) || misaligned(out) ||
       (reinterpret_cast<uintptr_t>(lse) & 3))
     return PSATTN_ERR_INVALID_ARG;
-  return psattn_launch_decode(hp, plan->dp, q, kv_pool, block_table, group_of_req, prefix_len,
-                              suffix_len, out, lse, stream);
+  const int rc = psattn_launch_decode(hp, plan->dp, q, kv_pool, block_table, group_of_req,
+                                     prefix_len, suffix_len, out, lse, stream);
+  if (rc) return rc;
+  // marks the end of this launch for psattn_plan_status and psattn_plan_destroy
+  if (cudaEventRecord(plan->done, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return PSATTN_ERR_CUDA;
+  }
+  return PSATTN_OK;
 }
 
 int psattn_plan_info_get(psattn_plan_t plan, psattn_plan_info* info) {
@@ -634,10 +662,20 @@ int psattn_plan_status(psattn_plan_t plan, uint32_t* device_flags) {
   if (device_flags) *device_flags = 0;
   if (!plan) return PSATTN_ERR_INVALID_ARG;
   if (!plan->on_device) return PSATTN_OK;
+  // Waits for the plan's last launch only (its event), then reads the error
+  // word on the plan's own stream, so other work on the device runs on.
   uint32_t w = 0;
-  if (cudaDeviceSynchronize() != cudaSuccess ||
-      cudaMemcpy(&w, plan->dp.ctr + kCtrErr, sizeof w, cudaMemcpyDeviceToHost) != cudaSuccess ||
-      cudaMemset(plan->dp.ctr + kCtrErr, 0, sizeof w) != cudaSuccess) {
+  cudaError_t e = cudaEventSynchronize(plan->done);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(&w, plan->dp.ctr + kCtrErr, sizeof w, cudaMemcpyDeviceToHost, plan->aux);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(plan->aux);
+  // A launch that raised the word may have ended with merge tickets that
+  // never reached their count (a bounded wait gave up, or the merge
+  // bookkeeping disagreed): the counters, tickets and the word itself all
+  // start again from zero, so the next launch cannot merge stale partials.
+  if (e == cudaSuccess && w) e = cudaMemsetAsync(plan->ws, 0, plan->reset_bytes, plan->aux);
+  if (e == cudaSuccess && w) e = cudaStreamSynchronize(plan->aux);
+  if (e != cudaSuccess) {
     cudaGetLastError();
     return PSATTN_ERR_CUDA;
   }
@@ -666,10 +704,7 @@ int psattn_selftest_wait_timeout(uint32_t limit_us, uint32_t* device_flags) {
 
 void psattn_plan_destroy(psattn_plan_t plan) {
   if (!plan) return;
-  if (plan->ws) {
-    cudaDeviceSynchronize();
-    cudaFree(plan->ws);
-  }
+  release_device(plan);  // waits for the plan's last launch first
   delete plan;
 }
 

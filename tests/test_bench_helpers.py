@@ -9,8 +9,6 @@ does not fail this test before the profiles are taken again.
 """
 import hashlib
 import os
-import types
-
 import pytest
 
 import bench
@@ -29,32 +27,35 @@ def _tree(tmp_path, src=b"kernel v1", recorded=None, bytes_line=True):
     return tmp_path
 
 
-def _args(**kw):
-    a = dict(workload="skewed", groups=None, no_fold=False, chunk_form="ragged")
-    a.update(kw)
-    return types.SimpleNamespace(**a)
+def _rec(workload="skewed", groups=None, no_fold=False, chunk_form="ragged"):
+    """bench._traffic_record as main() calls it for these arguments"""
+    return bench._traffic_record(workload, groups is None and not no_fold
+                                 and chunk_form == "ragged")
 
 
 def test_traffic_from_matching_summary(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(_tree(tmp_path)))
-    assert bench._traffic_record(_args()) == 123456789
+    traffic, source = _rec()
+    assert traffic == 123456789
+    assert source.startswith(os.path.join("profiles", "psattn_fused_decode_skewed.md"))
 
 
 @pytest.mark.parametrize("override", [dict(groups=8), dict(no_fold=True),
                                       dict(chunk_form="levels"), dict(workload="tiny_fp32")])
 def test_traffic_none_for_overrides_or_missing_summary(tmp_path, monkeypatch, override):
     monkeypatch.setattr(bench, "ROOT", str(_tree(tmp_path)))
-    assert bench._traffic_record(_args(**override)) is None
+    traffic, source = _rec(**override)
+    assert traffic is None and source.startswith("none")
 
 
 def test_traffic_none_for_stale_or_incomplete_summary(tmp_path, monkeypatch):
     root = _tree(tmp_path, src=b"kernel v2", recorded=b"kernel v1")
     monkeypatch.setattr(bench, "ROOT", str(root))
-    assert bench._traffic_record(_args()) is None
+    assert _rec()[0] is None
     other = tmp_path / "other"
     other.mkdir()
     monkeypatch.setattr(bench, "ROOT", str(_tree(other, bytes_line=False)))
-    assert bench._traffic_record(_args()) is None
+    assert _rec()[0] is None
 
 
 def test_oracle_threads():

@@ -211,6 +211,62 @@ def test_edge_empty_batch():
         assert pl.status() == (0, 0)
 
 
+def test_suffix_grows_across_blocks_without_replanning():
+    """A decode loop keeps its plan while every request's suffix grows by
+    1-40 tokens, crossing block boundaries: the new blocks go into spare
+    block-table columns (unused, -1, when the plan was built), and the kernel
+    reads lengths and block ids from the device tables of each launch."""
+    _lib()
+    import dataclasses
+    from workloads.device import DeviceProblem
+    p = W.make("llama8b", small=True, poison=False)
+    spare = 4  # 40 tokens need at most 3 more blocks
+    R, maxb = p.block_table.shape
+    bt = np.full((R, maxb + spare), -1, np.int32)
+    bt[:, :maxb] = p.block_table
+    nb0 = p.num_pool_blocks
+    growth = np.random.default_rng(8).integers(1, 41, size=R)
+    # enough new pool blocks for every request's new suffix blocks
+    new_blocks = [-(-(int(s) + int(g)) // 16) - -(-int(s) // 16)
+                  for s, g in zip(p.suffix_len, growth)]
+    extra = sum(new_blocks)
+    pool = np.concatenate([p.pool, np.zeros((extra,) + p.pool.shape[1:], p.pool.dtype)])
+    rng = np.random.default_rng(9)
+    pool[nb0:] = W.f32_to_bf16_bits(rng.standard_normal(pool[nb0:].shape, dtype=np.float32))
+    p = dataclasses.replace(p, block_table=bt, pool=pool)
+    d = DeviceProblem(p)
+    with d.plan() as pl:
+        # step 1: the planned batch
+        d.decode(pl)
+        out0, lse0 = d.result()
+        assert pl.status() == (0, 0)
+        _check(p, out0, lse0)
+        # step 2: the same plan after the suffixes grew
+        grown_bt = bt.copy()
+        grown_len = p.suffix_len.copy()
+        nxt = nb0
+        for r in range(R):
+            used = int(np.count_nonzero(bt[r] >= 0))
+            for k in range(new_blocks[r]):
+                grown_bt[r, used + k] = nxt
+                nxt += 1
+            s0 = int(p.suffix_len[r])
+            grown_len[r] = s0 + int(growth[r])
+            # the tokens past the old end inside the old last block get new values
+            if s0 % 16:
+                blk = bt[r, used - 1]
+                pool[blk, :, :, s0 % 16:, :] = W.f32_to_bf16_bits(
+                    rng.standard_normal((2, p.num_kv_heads, 16 - s0 % 16, p.head_dim),
+                                        dtype=np.float32))
+        assert nxt == pool.shape[0]
+        p2 = dataclasses.replace(p, block_table=grown_bt, suffix_len=grown_len, pool=pool)
+        d2 = DeviceProblem(p2)
+        d2.decode(pl)
+        out, lse = d2.result()
+        assert pl.status() == (0, 0)
+    _check(p2, out, lse)
+
+
 def test_suffix_grows_without_replanning():
     _lib()
     from workloads.device import DeviceProblem
@@ -257,8 +313,10 @@ def test_device_error_word_on_bad_block_id():
         bt[5, int(np.count_nonzero(bt[5] >= 0)) - 1] = p.num_pool_blocks + 1000
         d.bt.copy_(torch.from_numpy(bt))
         d.decode(pl)
+        d.decode(pl)
         rc, flags = pl.status()
         assert rc == -7 and flags & 1
+        # the error word, counters and tickets were reset by the status read
         # the plan still works once the table is fixed
         d.bt.copy_(torch.from_numpy(p.block_table))
         d.decode(pl)
@@ -297,10 +355,31 @@ def _sample(p, n=40):
     return sorted(picks)
 
 
-@pytest.mark.parametrize("name", FULL)
-def test_parity_full_size_sampled(name):
-    _lib()
+@pytest.mark.parametrize("name,flag", [(n, "0") for n in FULL] + [("two_level", "NO_FOLD")])
+def test_parity_full_size_sampled(name, flag):
+    """Sampled requests of every full-size batch, in the benchmark's launch
+    configuration.  The two-level batch also runs as the three-partial merge
+    (NO_FOLD: level 1, the request's level-2 group and its suffix are each a
+    partial of their own, merged in the same launch)."""
+    ps = _lib()
     p = W.make(name)
-    out, lse = _run(p)
+    out, lse = _run(p, 0 if flag == "0" else getattr(ps, flag))
     _check(p, out, lse, _sample(p))
     assert np.isfinite(out).all() and np.isfinite(lse).all()
+
+
+def test_no_fold_plan_has_three_partials_per_request():
+    """The NO_FOLD plan of the full-size two-level batch is the literal
+    three-partial form: every request merges level 1, its level-2 group and
+    its suffix chunks, and the dense items read level 1 and level 2
+    separately."""
+    ps = _lib()
+    from workloads.device import shape_of
+    p = W.make("two_level", poison=False)
+    with ps.Plan(shape_of(p), p.block_table, p.group_of_req, p.group_parent, p.prefix_len,
+                 p.suffix_len, flags=ps.NO_FOLD, host_only_sms=152) as pl:
+        req = pl.export(ps.EXPORT_REQ).reshape(-1, 8)
+        grp = pl.export(ps.EXPORT_GROUP).reshape(-1, 8)
+    n_suffix_chunks = req[:, 4]
+    assert (req[:, 1] == grp[0, 2] + grp[1, 2] + n_suffix_chunks).all()
+    assert grp[0, 2] >= 1 and grp[1, 2] >= 1 and (n_suffix_chunks >= 1).all()

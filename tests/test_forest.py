@@ -146,6 +146,38 @@ def test_worked_example():
     assert single["saved_tokens"] == brute_single(reqs, 2) == 8  # all three at 4 tokens beat 2 at 6
 
 
+def test_page_example_first_level_reuse():
+    """BatchLLM section 4.2's worked example (tests/golden): the naive first
+    level ('b' shared by prompts 2-6) saves 4 tokens; the enlargement must
+    instead keep prompts 4 and 5 together on their shared 8 tokens, which the
+    page says saves 8.  Both numbers are the page's; the DP's total here also
+    groups prompts 2, 3 and 6 on 'b' (2 more tokens), and exhaustive
+    enumeration agrees that this is the optimum."""
+    import json
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "batchllm_first_level_reuse.json")
+    case = json.load(open(path))
+    reqs, chunk, stated = case["prompts"], case["chunk"], case["stated"]
+    # the compact tree's first level: the root's children
+    multi = check_multilevel(reqs, chunk)
+    roots = [g for g in range(len(multi["prefix_len"])) if multi["group_parent"][g] == -1]
+    assert len(roots) == 1
+    first = roots[0]
+    through = [r for r, ch in enumerate(chains(multi)) if first in ch]
+    assert through == stated["first_level_prompts"]
+    assert (len(through) - 1) * int(multi["prefix_len"][first]) == stated["first_level_saving"]
+    # the enlarged single level keeps the pair on its 8 shared tokens
+    single = check_single(reqs, chunk)
+    a, b = stated["pair"]
+    g = int(single["group_of_req"][a])
+    assert g >= 0 and int(single["group_of_req"][b]) == g
+    assert [r for r in range(len(reqs)) if single["group_of_req"][r] == g] == [a, b]
+    assert int(single["prefix_len"][g]) == stated["pair_shared_tokens"]
+    assert (2 - 1) * int(single["prefix_len"][g]) == stated["pair_saving"]
+    assert single["saved_tokens"] > stated["first_level_saving"]
+    assert single["saved_tokens"] == brute_single(reqs, chunk) == stated["pair_saving"] + 2
+
+
 def test_enlargement_beats_the_deepest_level():
     # two requests share 6 chunks, a third shares only the first 5 with them:
     # grouping all three at 5 chunks saves 2 * 5 = 10 > 1 * 6

@@ -196,15 +196,19 @@ def test_gather_exact_small(name, flag):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("name", ["llama8b", "long_prefix", "skewed", "two_level"])
-def test_gather_exact_full_size(name):
+@pytest.mark.parametrize("name,flag", [("llama8b", "0"), ("long_prefix", "0"), ("skewed", "0"),
+                                       ("two_level", "0"), ("two_level", "NO_FOLD")])
+def test_gather_exact_full_size(name, flag):
     """Every output of the full-size batch, in the benchmark's launch
-    configuration."""
+    configuration.  The two-level batch also runs with every level its own
+    partial (NO_FOLD): its 4096 requests then merge three partials each (the
+    shared level 1, their level-2 group, their suffix) in the one launch."""
     pytest.importorskip("torch")
+    import shared_prefix_kv_gb300 as ps
     p = W.make(name)
     q, want, want_lse = one_hot(p, seed=4)
     p = dataclasses.replace(p, q=q)
-    out, lse = _run_decode(p, 0)
+    out, lse = _run_decode(p, 0 if flag == "0" else getattr(ps, flag))
     _compare(p, out, lse, want, want_lse)
 
 

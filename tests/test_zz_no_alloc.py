@@ -21,10 +21,12 @@ torch = pytest.importorskip("torch")
 
 
 def test_noalloc_matches_decode_two_calls():
+    import oracle
     import shared_prefix_kv_gb300 as ps
     from workloads.device import DeviceProblem, shape_of, tolerances
 
     p = W.make("llama8b", small=True)
+    o_ref, l_ref = oracle.attention(p)
     d = DeviceProblem(p)
     with d.plan() as pl:
         d.decode(pl)
@@ -44,6 +46,8 @@ def test_noalloc_matches_decode_two_calls():
             assert np.isfinite(out).all() and np.isfinite(lse).all()
             assert np.abs(out - ref_out).max() <= t_out
             assert np.abs(lse - ref_lse).max() <= t_lse
+            assert np.abs(out - o_ref).max() <= t_out
+            assert np.abs(lse - l_ref).max() <= t_lse
 
 
 def test_noalloc_ragged_chunked_batch():
