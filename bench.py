@@ -283,6 +283,8 @@ def _config(args, p):
         desc += f" (groups overridden to {args.groups})"
     if getattr(args, "no_fold", False):
         desc += " (planned with no folding: every prefix level its own partial)"
+    if getattr(args, "plan_flag", None):
+        desc += " (plan flags: " + ", ".join(args.plan_flag) + ")"
     return {"workload": f"{args.workload}: {desc}",
             "requests_per_gpu": p.num_req, "global_batch": p.num_req * args.gpus,
             "parallelism": f"replicas x{args.gpus} (independent batches)",
@@ -415,6 +417,10 @@ def main():
                          "levels into their children's tensor-core items)")
     ap.add_argument("--no-baselines", action="store_true",
                     help="skip the CPU-oracle, no-dedup and end-to-end legs")
+    ap.add_argument("--plan-flag", action="append", default=[],
+                    choices=["SIMT", "NO_TENSOR_PREFIX", "FLATTEN", "NO_FOLD"],
+                    help="extra plan flag for the headline launch (repeatable), e.g. SIMT for "
+                         "the CUDA-core per-warp path")
     ap.add_argument("--no-per-workload", action="store_true",
                     help="skip the per_workload block (every configuration's own "
                          "measurement, single-GPU runs only)")
@@ -443,7 +449,10 @@ def main():
     alg_override = chunk_info[0] if chunk_info else None
     d = DeviceProblem(p)
     t_plan = time.perf_counter()
-    plan = d.plan(ps.NO_FOLD if args.no_fold else 0)
+    plan_flags = ps.NO_FOLD if args.no_fold else 0
+    for f in args.plan_flag:
+        plan_flags |= getattr(ps, f)
+    plan = d.plan(plan_flags)
     t_plan = time.perf_counter() - t_plan
     info = plan.info()
     stream = torch.cuda.current_stream()
@@ -483,7 +492,8 @@ def main():
     peak, peak_kind = _peak_hbm()
     achieved = alg_bytes / (ms * 1e-3) / 1e9
     traffic, traffic_src = _traffic_record(
-        args.workload, args.groups is None and not args.no_fold and args.chunk_form == "ragged")
+        args.workload, args.groups is None and not args.no_fold and args.chunk_form == "ragged"
+        and not args.plan_flag)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -111,6 +111,37 @@ int psattn_cht_batches(const int32_t* tokens, const int64_t* offsets, int32_t nu
                        int32_t chunk, int32_t max_batch, int32_t max_new_chunks,
                        int32_t* batch_of_req, int32_t* order, int32_t* num_batches);
 
+/* The chunked-hash-tree batches of psattn_cht_batches, each turned into the
+ * grouping metadata psattn_plan consumes (Feather, methodology 1, forms the
+ * prefix-homogeneous batches; within a batch the requests are grouped by
+ * their shared chunk-prefixes exactly as psattn_forest_group groups a batch
+ * of its own, with the same flags).
+ *
+ * Batch b's requests, in increasing id order, form its own group forest:
+ * its groups are the ids [batch_group_offset[b], batch_group_offset[b + 1]),
+ * a group's parent is a group of the same batch (or -1), and a request's
+ * group is one of its batch's (or -1).  To plan batch b, take its requests
+ * and subtract batch_group_offset[b] from their group ids and from the
+ * parents of its groups.
+ *
+ *  batch_of_req, order, num_batches   as psattn_cht_batches.
+ *  batch_group_offset  int32 [num_req + 1] out (num_batches + 1 entries used).
+ *  group_of_req, suffix_len  int32 [num_req] out.
+ *  group_parent, prefix_len  int32 [cap] out; PSATTN_ERR_NOMEM (with
+ *                *num_groups = the number needed) when cap is too small;
+ *                num_req - 1 always suffices.
+ *  saved_tokens  out (may be NULL): sum of the batches' savings as defined
+ *                for psattn_forest_group.
+ * Errors: PSATTN_ERR_INVALID_ARG as psattn_cht_batches and psattn_forest_group
+ * (NULL pointer, num_req < 0, chunk < 1, max_batch < 1, max_new_chunks < 0,
+ * decreasing offsets, unknown flags). */
+int psattn_cht_group(const int32_t* tokens, const int64_t* offsets, int32_t num_req,
+                     int32_t chunk, int32_t max_batch, int32_t max_new_chunks, uint32_t flags,
+                     int32_t* batch_of_req, int32_t* order, int32_t* num_batches,
+                     int32_t* batch_group_offset, int32_t* group_of_req, int32_t* group_parent,
+                     int32_t* prefix_len, int32_t* suffix_len, int32_t cap, int32_t* num_groups,
+                     int64_t* saved_tokens);
+
 #ifdef __cplusplus
 }
 #endif

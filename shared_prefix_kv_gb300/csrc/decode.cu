@@ -705,8 +705,8 @@ constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;  // kStages V stages
 constexpr uint32_t kOffE = kOffK;
 static_assert(128 * 128 * 4 <= kStages * kTileBytes, "O staging overruns the K stages");
 constexpr int kMaxDenseBlocks = 512;                    // chunk <= 8192 tokens
-constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;  // 20 mbarriers
-constexpr uint32_t kOffMisc = kOffBar + 160;
+constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;  // 21 mbarriers
+constexpr uint32_t kOffMisc = kOffBar + 168;
 constexpr uint32_t kDenseSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
 static_assert(kDenseSmemBytes <= 232448, "dense tile shared memory exceeds 227 KB");
 constexpr uint32_t kTmemCols = 512;
@@ -928,6 +928,7 @@ struct DenseState {
   uint32_t sbase;      // its shared-space address
   uint32_t tmem;       // TMEM base address
   uint32_t g;          // tiles this CTA has run so far (drives every ring phase)
+  uint32_t xph;        // completions of the softmax threads' exchange barrier so far
   volatile int* abort;
   // softmax threads: the item's member tickets (lane mu: member mu's unit
   // r * Hkv + h and partial count)
@@ -950,6 +951,8 @@ struct DenseState {
 //                     other one and cannot complete a phase for a tile the
 //                     slower warps have not finished)
 //   pfree[b]          PV of P buffer b done (P may be rewritten; O updated)
+//   x                 all 128 softmax threads reached the same point of an
+//                     item's epilogue (the exchange between row copies)
 __device__ __forceinline__ uint32_t bar_k(const DenseState& d, uint32_t st) { return d.sbase + kOffBar + 8u * st; }
 __device__ __forceinline__ uint32_t bar_v(const DenseState& d, uint32_t st) { return d.sbase + kOffBar + 24u + 8u * st; }
 __device__ __forceinline__ uint32_t bar_s(const DenseState& d, uint32_t b) { return d.sbase + kOffBar + 48u + 8u * b; }
@@ -958,6 +961,18 @@ __device__ __forceinline__ uint32_t bar_p(const DenseState& d, uint32_t b) { ret
 __device__ __forceinline__ uint32_t bar_pfree(const DenseState& d, uint32_t b) { return d.sbase + kOffBar + 96u + 8u * b; }
 __device__ __forceinline__ uint32_t bar_kfree(const DenseState& d, uint32_t st) { return d.sbase + kOffBar + 112u + 8u * st; }
 __device__ __forceinline__ uint32_t bar_vfree(const DenseState& d, uint32_t st) { return d.sbase + kOffBar + 136u + 8u * st; }
+__device__ __forceinline__ uint32_t bar_x(const DenseState& d) { return d.sbase + kOffBar + 160u; }
+
+// Row copies of a small dense item.  An item of at most 32 (64) q rows runs
+// each row as 4 (2) copies in the four (two) TMEM lane quadrants: copy c of
+// row rho sits at lane c * width + rho and takes only the tile columns
+// [c * width, (c + 1) * width) of every tile, with its own running max, sum
+// and O.  Each softmax thread then passes over 32 (64) columns of a tile
+// instead of 128, and the copies are merged by their maxima in the epilogue
+// (the online-softmax combination of partials over disjoint token sets).
+__device__ __forceinline__ int copy_width(int nrows) {
+  return nrows <= 32 ? 32 : (nrows <= 64 ? 64 : kTileTok);
+}
 
 // Block-table lookup for the K or V tile of local tile j, by the 32 lanes of a
 // producer warp: lanes 0-15 each take one of the tile's 8 blocks (lane / 2)
@@ -1076,17 +1091,19 @@ __device__ void producer_item(const Params& P, DenseState& d, const Span& s, int
 }
 
 // The Q tile of one item (threads 0-127); returns the request of the
-// thread's row (-1 past the item's rows).
+// thread's row (-1 past the item's rows).  Tile row t holds q row t % width
+// (copy_width): small items repeat their rows in every lane quadrant.
 __device__ int prepare_item(const Params& P, DenseState& d, const Item& it, int nrows) {
   const int tid = threadIdx.x, G = P.G, h = it.kvh;
+  const int rho = tid % copy_width(nrows);
   // Q tile, K-major, 128B swizzle: 16-byte chunk c of row t at
   // atom (c / 8), row t, position (c % 8) ^ (t % 8)
   uint8_t* qs = d.smem + kOffQ;
   const __nv_bfloat16* qp = nullptr;
   int r = -1;
-  if (tid < nrows) {
-    r = member_req(P, it, tid / G);
-    qp = reinterpret_cast<const __nv_bfloat16*>(P.q) + ((size_t)r * P.Hq + h * G + tid % G) * 128;
+  if (rho < nrows) {
+    r = member_req(P, it, rho / G);
+    qp = reinterpret_cast<const __nv_bfloat16*>(P.q) + ((size_t)r * P.Hq + h * G + rho % G) * 128;
   }
 #pragma unroll
   for (int c = 0; c < 16; ++c) {
@@ -1097,13 +1114,15 @@ __device__ int prepare_item(const Params& P, DenseState& d, const Item& it, int 
   return r;
 }
 
-// Row max of S(g) (scaled to log2 units) over the tile's valid columns.
+// Row max of S(g) (scaled to log2 units) over the valid columns of the NQ
+// groups of 32 columns at sa.
+template <int NQ>
 __device__ __forceinline__ float tile_max(uint32_t sa, float sl2, int tile_valid) {
   float mxa[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) mxa[i] = -INFINITY;
 #pragma unroll
-  for (int q4 = 0; q4 < 4; ++q4) {
+  for (int q4 = 0; q4 < NQ; ++q4) {
     float v[32];
     tmem_ld32(sa + q4 * 32, v);
 #pragma unroll
@@ -1114,12 +1133,12 @@ __device__ __forceinline__ float tile_max(uint32_t sa, float sl2, int tile_valid
                fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7]))) * sl2;
 }
 
-// One pass over S(g) of this thread's row: P = 2^(s * sl2 - m) as bf16 pairs
-// into the row's TMEM lane at pa (token 2c and 2c + 1 in column c, the lower
-// token in the low half), columns past tile_valid as 0 (kFull: all 128
-// columns are valid, no masks).  Returns the row sum of P (fp32).  The next
-// 32 columns of S are loaded while this 32 are computed.
-template <bool kFull>
+// One pass over NQ x 32 columns of S(g) of this thread's row: P = 2^(s * sl2
+// - m) as bf16 pairs into the row's TMEM lane at pa (token 2c and 2c + 1 in
+// column c, the lower token in the low half), columns past tile_valid as 0
+// (kFull: every column is valid, no masks).  Returns the row sum of P (fp32).
+// The next 32 columns of S are loaded while this 32 are computed.
+template <int NQ, bool kFull>
 __device__ __forceinline__ float softmax_pass(uint32_t sa, float sl2, float m, int tile_valid,
                                               uint32_t pa) {
   const float2 sl2_2 = make_float2(sl2, sl2), negm_2 = make_float2(-m, -m);
@@ -1128,8 +1147,8 @@ __device__ __forceinline__ float softmax_pass(uint32_t sa, float sl2, float m, i
   tmem_ld32_async(sa, r[0]);
   tmem_wait_ld();
 #pragma unroll
-  for (int q4 = 0; q4 < 4; ++q4) {
-    if (q4 + 1 < 4) tmem_ld32_async(sa + (q4 + 1) * 32, r[(q4 + 1) & 1]);
+  for (int q4 = 0; q4 < NQ; ++q4) {
+    if (q4 + 1 < NQ) tmem_ld32_async(sa + (q4 + 1) * 32, r[(q4 + 1) & 1]);
     const uint32_t* v = r[q4 & 1];
     uint32_t pk[16];
 #pragma unroll
@@ -1147,44 +1166,58 @@ __device__ __forceinline__ float softmax_pass(uint32_t sa, float sl2, float m, i
       pk[e >> 1] = *reinterpret_cast<const uint32_t*>(&pp);
     }
     tmem_st16(pa + q4 * 16, pk);
-    if (q4 + 1 < 4) tmem_wait_ld();
+    if (q4 + 1 < NQ) tmem_wait_ld();
   }
   tmem_wait_st();
   return (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
 }
 
-// Both passes are separate functions: scheduled on their own, away from the
+// The passes are separate functions: scheduled on their own, away from the
 // rest of the kernel, the full pass runs about twice as fast.
+template <int NQ>
 __device__ __noinline__ float softmax_pass_full(uint32_t sa, float sl2, float m, uint32_t pa) {
-  return softmax_pass<true>(sa, sl2, m, kTileTok, pa);
+  return softmax_pass<NQ, true>(sa, sl2, m, NQ * 32, pa);
 }
+template <int NQ>
 __device__ __noinline__ float softmax_pass_masked(uint32_t sa, float sl2, float m, int tile_valid,
                                                   uint32_t pa) {
-  return softmax_pass<false>(sa, sl2, m, tile_valid, pa);
+  return softmax_pass<NQ, false>(sa, sl2, m, tile_valid, pa);
 }
 
-// tile_valid may differ between the warp's rows (a ragged leaf level); the
-// pass is chosen for the whole warp (tcgen05.ld is warp-collective)
-__device__ __forceinline__ float softmax_pass_any(uint32_t sa, float sl2, float m, int tile_valid,
-                                                  uint32_t pa) {
-  return __all_sync(0xffffffffu, tile_valid == kTileTok)
-             ? softmax_pass_full(sa, sl2, m, pa)
-             : softmax_pass_masked(sa, sl2, m, tile_valid, pa);
+// nq (4, 2 or 1 groups of 32 columns) is the same in every thread of the
+// item.  tile_valid may differ between the warp's rows (a ragged leaf
+// level); full or masked is chosen for the whole warp (tcgen05.ld is
+// warp-collective).
+__device__ __forceinline__ float softmax_pass_any(int nq, uint32_t sa, float sl2, float m,
+                                                  int tile_valid, uint32_t pa) {
+  const bool full = __all_sync(0xffffffffu, tile_valid == nq * 32);
+  if (nq == 4) return full ? softmax_pass_full<4>(sa, sl2, m, pa)
+                           : softmax_pass_masked<4>(sa, sl2, m, tile_valid, pa);
+  if (nq == 2) return full ? softmax_pass_full<2>(sa, sl2, m, pa)
+                           : softmax_pass_masked<2>(sa, sl2, m, tile_valid, pa);
+  return full ? softmax_pass_full<1>(sa, sl2, m, pa)
+              : softmax_pass_masked<1>(sa, sl2, m, tile_valid, pa);
+}
+
+__device__ __forceinline__ float tile_max_any(int nq, uint32_t sa, float sl2, int tile_valid) {
+  if (nq == 4) return tile_max<4>(sa, sl2, tile_valid);
+  if (nq == 2) return tile_max<2>(sa, sl2, tile_valid);
+  return tile_max<1>(sa, sl2, tile_valid);
 }
 
 // Cold path of the softmax: some row's tile sum of P outgrew the limit (its
 // running max is stale).  Recompute P for the warp (rows that did not grow keep their
 // max), then rescale O and l of the grown rows once PV(g - 1) is complete.
-__device__ __noinline__ bool softmax_regrow(const Params& P, DenseState& d, uint32_t sa,
+__device__ __noinline__ bool softmax_regrow(const Params& P, DenseState& d, int nq, uint32_t sa,
                                             uint32_t trow, int tile_valid, uint32_t pa,
                                             uint32_t g, bool grow, float* m_run, float* l_run,
                                             float* psum) {
   // tcgen05.ld is warp-collective: every lane reads the tile max, then selects
-  const float tmax = tile_max(sa, P.sl2, tile_valid);
+  const float tmax = tile_max_any(nq, sa, P.sl2, tile_valid);
   const float m_new = grow ? tmax : *m_run;
   // equal maxima (also a row that has seen no token: both -inf) need no rescale
   const float alpha = (m_new == *m_run) ? 1.f : ex2(*m_run - m_new);
-  *psum = softmax_pass_any(sa, P.sl2, m_new, tile_valid, pa);
+  *psum = softmax_pass_any(nq, sa, P.sl2, m_new, tile_valid, pa);
   // PV(g - 1) done: pfree of its buffer, completion (g - 1) / 2
   if (!mbar_wait(bar_pfree(d, (g - 1) & 1), ((g - 1) >> 1) & 1, d.abort)) return false;
   tc_fence_after();
@@ -1362,11 +1395,33 @@ __device__ void settle_tickets(const Params& P, DenseState& d, MergeRing& ring) 
 // The softmax warps' part of one item, then the epilogue.  r_row is the
 // request of this thread's row (-1 past the item's rows).  Returns early
 // (abort set) on a timeout.
+// All 128 softmax threads at the same point (bounded; false on abort).
+__device__ __forceinline__ bool softmax_threads_sync(DenseState& d) {
+  mbar_arrive(bar_x(d));
+  const bool ok = mbar_wait(bar_x(d), d.xph & 1, d.abort);
+  ++d.xph;
+  return ok;
+}
+
 __device__ void softmax_item(const Params& P, DenseState& d, MergeRing& ring, const Item& it,
                              int t0, int ntok, int ntiles, int nrows, int r_row) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t g0 = d.g;
   const uint32_t trow = d.tmem + ((uint32_t)(warp * 32) << 16);
+  // this thread's row copy: tile columns [col0, col0 + cw) of every tile
+  const int cw = copy_width(nrows), nq = cw / 32, ncopy = kTileTok / cw;
+  const int col0 = (tid / cw) * cw;
+  if (ncopy > 1) {
+    // P columns outside a copy's slice stay 0 for the whole item, so each
+    // copy's PV sums only its own tokens.  Both P buffers are idle here: the
+    // previous item waited for its last PV.
+    uint32_t z[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) z[i] = 0u;
+#pragma unroll
+    for (int c = 0; c < 128; c += 16) tmem_st16(trow + kTmemP + c, z);
+    tmem_wait_st();
+  }
   // the row's partial slots, needed only at the end (the load hides behind the tiles)
   // row_end: tokens of the item's span the row attends to (fewer than the
   // span only on a ragged leaf level, whose members see its first leaf_vis
@@ -1382,21 +1437,22 @@ __device__ void softmax_item(const Params& P, DenseState& d, MergeRing& ring, co
   for (int j = 0; j < ntiles; ++j) {
     const uint32_t g = g0 + j, b = g & 1;
     const int tile_valid = min(kTileTok, ntok - j * kTileTok);  // the item's tokens (V rows)
-    const int row_valid = max(0, min(tile_valid, row_end - j * kTileTok));  // this row's
-    const uint32_t pa = trow + kTmemP + b * 64;
+    // this row copy's valid columns of its slice
+    const int row_valid = max(0, min(cw, min(tile_valid, row_end - j * kTileTok) - col0));
+    const uint32_t pa = trow + kTmemP + b * 64 + col0 / 2;
     if (!mbar_wait(bar_s(d, b), (g >> 1) & 1, d.abort)) return;
     // P buffer b was last read by PV(g - 2)
     if (j >= 2 && !mbar_wait(bar_pfree(d, b), ((g >> 1) - 1) & 1, d.abort)) return;
     tc_fence_after();
-    const uint32_t sa = trow + b * 128;
+    const uint32_t sa = trow + b * 128 + col0;
     // P against the running max (the tile's own max on the first tile of the
     // item, when O is still empty); rows whose tile sum outgrew the limit are
     // redone with their new max (rare)
-    if (j == 0) m_run = tile_max(sa, P.sl2, row_valid);
-    float psum = softmax_pass_any(sa, P.sl2, m_run, row_valid, pa);
+    if (j == 0) m_run = tile_max_any(nq, sa, P.sl2, row_valid);
+    float psum = softmax_pass_any(nq, sa, P.sl2, m_run, row_valid, pa);
     const bool grow = psum > kRescaleSumLimit;
     if (j > 0 && __any_sync(0xffffffffu, grow)) {
-      if (!softmax_regrow(P, d, sa, trow, row_valid, pa, g, grow, &m_run, &l_run, &psum))
+      if (!softmax_regrow(P, d, nq, sa, trow, row_valid, pa, g, grow, &m_run, &l_run, &psum))
         return;
     }
     l_run = (j == 0) ? psum : l_run + psum;
@@ -1442,6 +1498,22 @@ __device__ void softmax_item(const Params& P, DenseState& d, MergeRing& ring, co
   const int G = P.G, h = it.kvh;
   float* E = reinterpret_cast<float*>(d.smem + kOffE);
   fence_proxy_async();  // E overlays K stages the TMA and the tensor cores used
+  // Row copies: the row's maximum over its copies, each copy's O and l
+  // scaled to it; copy 0's warps then write the sums (the V stages are idle
+  // and hold the exchange).
+  float fac = 1.f, m_out = m_run, l_out = l_run;
+  float* X = reinterpret_cast<float*>(d.smem + kOffV);  // [2][128]: m, then scaled l
+  const int rho = tid % cw;
+  if (ncopy > 1) {
+    X[tid] = m_run;
+    if (!softmax_threads_sync(d)) return;
+    float mx = -INFINITY;
+    for (int c = 0; c < ncopy; ++c) mx = fmaxf(mx, X[rho + c * cw]);
+    // a copy that saw no token (m = -inf, O = 0, l = 0) adds nothing
+    fac = (m_run == -INFINITY) ? 0.f : ex2(m_run - mx);
+    X[128 + tid] = l_run * fac;
+    m_out = mx;
+  }
 #pragma unroll
   for (int q4 = 0; q4 < 4; ++q4) {
     float o[32];
@@ -1455,32 +1527,66 @@ __device__ void softmax_item(const Params& P, DenseState& d, MergeRing& ring, co
     for (int e = 0; e < 32; e += 4) {
       const int c = q4 * 8 + (e >> 2);
       *reinterpret_cast<float4*>(E + tid * 128 + ((c ^ (tid & 7)) << 2)) =
-          make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+          make_float4(o[e] * fac, o[e + 1] * fac, o[e + 2] * fac, o[e + 3] * fac);
     }
   }
-  if (tid < nrows && r_row >= 0)
+  if (ncopy > 1) {
+    if (!softmax_threads_sync(d)) return;  // every copy's E rows and l written
+    l_out = 0.f;
+    for (int c = 0; c < ncopy; ++c) l_out += X[128 + rho + c * cw];
+  }
+  // copy 0 (threads below cw) writes the row's partial.  A member whose
+  // (request, KV head) unit has this one partial gets its output and LSE
+  // here instead: no partial slot, no ticket, no merge.
+  const bool writer = tid < cw;
+  float2* Y = reinterpret_cast<float2*>(d.smem + kOffV + 1024);  // [128]: the rows' m, l
+  Y[tid] = make_float2(m_out, l_out);
+  if (writer && tid < nrows && r_row >= 0 && np_row > 1)
     __stcg(&P.dp.mlpart[(((size_t)sb_row + it.slot_j) * P.Hkv + h) * G + tid % G],
-           make_float2(m_run, l_run));
+           make_float2(m_out, l_out));
   tc_fence_before();
   __syncwarp();
   // this warp's members: lane mu speaks for member mu (rows warp * 32 + mu * G ..)
   const int mpw = 32 / G, src = (lane < mpw ? lane : 0) * G;
   const int sb_m = __shfl_sync(0xffffffffu, sb_row, src);
+  const int r_m = __shfl_sync(0xffffffffu, r_row, src);
+  const int np_m = __shfl_sync(0xffffffffu, np_row, src);
   for (int mu = 0; mu < mpw; ++mu) {
     const int row0 = warp * 32 + mu * G;
-    if (row0 >= nrows) break;
+    if (row0 >= nrows || warp * 32 >= cw) break;
     const int sbm = __shfl_sync(0xffffffffu, sb_m, mu);
+    const int rm = __shfl_sync(0xffffffffu, r_m, mu);
+    const bool only = __shfl_sync(0xffffffffu, np_m, mu) == 1;
     float* dst = P.dp.opart + ((((size_t)sbm + it.slot_j) * P.Hkv + h) * G) * 128;
     for (int x = lane; x < G * 32; x += 32) {
       const int rr = x >> 5, c = x & 31, row = row0 + rr;
-      __stcg(reinterpret_cast<float4*>(dst + rr * 128 + c * 4),
-             *reinterpret_cast<const float4*>(E + row * 128 + ((c ^ (row & 7)) << 2)));
+      float4 v = *reinterpret_cast<const float4*>(E + row * 128 + ((c ^ (row & 7)) << 2));
+      for (int k = 1; k < ncopy; ++k) {
+        const int rk = row + k * cw;
+        const float4 w = *reinterpret_cast<const float4*>(E + rk * 128 + ((c ^ (rk & 7)) << 2));
+        v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
+      }
+      if (!only) {
+        __stcg(reinterpret_cast<float4*>(dst + rr * 128 + c * 4), v);
+        continue;
+      }
+      if (rm < 0) continue;
+      const float2 ml = Y[row];
+      const bool empty = !(ml.y > 0.f);
+      const float inv = empty ? 0.f : 1.f / ml.y;
+      const int hq = h * G + rr;
+      __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(P.out) + ((size_t)rm * P.Hq + hq) * 128;
+      *reinterpret_cast<uint2*>(o + c * 4) =
+          make_uint2(pack_bf16(v.x * inv, v.y * inv), pack_bf16(v.z * inv, v.w * inv));
+      if (c == 0) {
+        if (empty) raise(P, kErrEmpty);
+        if (P.lse) P.lse[(size_t)rm * P.Hq + hq] = empty ? -INFINITY : (ml.x + __log2f(ml.y)) * kLn2;
+      }
     }
   }
-  // lane mu takes member mu's ticket; the last arriver of a unit queues its merge
-  const int r_m = __shfl_sync(0xffffffffu, r_row, src);
-  const int np_m = __shfl_sync(0xffffffffu, np_row, src);
-  d.pend_valid = lane < mpw && warp * 32 + lane * G < nrows && r_m >= 0;
+  // lane mu takes member mu's ticket (units with more than one partial); the
+  // last arriver of a unit queues its merge
+  d.pend_valid = writer && lane < mpw && warp * 32 + lane * G < nrows && r_m >= 0 && np_m > 1;
   d.pend_unit = (uint32_t)(d.pend_valid ? r_m : 0) * P.Hkv + h;
   d.pend_np = np_m;
   d.pend_any = 1;
@@ -1497,6 +1603,7 @@ __device__ void dense_loop(const Params& P, uint8_t* smem_raw, MergeRing& ring) 
   d.smem = smem_raw + pad;
   d.sbase = raw + pad;
   d.g = 0;
+  d.xph = 0;
   d.pend_unit = 0;
   d.pend_np = 0;
   d.pend_valid = 0;
@@ -1518,6 +1625,7 @@ __device__ void dense_loop(const Params& P, uint8_t* smem_raw, MergeRing& ring) 
       mbar_init(bar_p(d, b), 4);
       mbar_init(bar_pfree(d, b), 1);
     }
+    mbar_init(bar_x(d), 128);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) {
@@ -1581,9 +1689,19 @@ __device__ void dense_loop(const Params& P, uint8_t* smem_raw, MergeRing& ring) 
 
 // ------------------------------------------------------------ the launch
 
+// PSATTN_SUFFIX_SIMT=1 (build define, for measurement): on the bf16 d = 128
+// path, suffix items run on the CUDA-core item (shuffle-reduced dot
+// products) instead of mma.sync, everything else unchanged.
+#ifndef PSATTN_SUFFIX_SIMT
+#define PSATTN_SUFFIX_SIMT 0
+#endif
+
 template <int PATH>
 __device__ __forceinline__ void run_item(const Params& P, const Item& it, int lane) {
-  if constexpr (PATH == kPathMmaBf16D128) mma_item(P, it, lane);
+  if constexpr (PATH == kPathMmaBf16D128 && PSATTN_SUFFIX_SIMT) {
+    if (it.kind == kItemSuffix && P.G <= kSimtRows) simt_item<__nv_bfloat16, 128>(P, it, lane);
+    else mma_item(P, it, lane);
+  } else if constexpr (PATH == kPathMmaBf16D128) mma_item(P, it, lane);
   else if constexpr (PATH == kPathSimtF32D64) simt_item<float, 64>(P, it, lane);
   else if constexpr (PATH == kPathSimtF32D128) simt_item<float, 128>(P, it, lane);
   else if constexpr (PATH == kPathSimtBf16D64) simt_item<__nv_bfloat16, 64>(P, it, lane);

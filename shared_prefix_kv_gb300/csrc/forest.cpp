@@ -373,6 +373,56 @@ void cht_batches(const Requests& q, const std::vector<std::vector<uint64_t>>& h,
   *num_batches = nb;
 }
 
+// Groups one set of requests (the body of psattn_forest_group): fills
+// group_of_req / suffix_len per request and group_parent / prefix_len per
+// group, and the saved tokens.
+struct Grouping {
+  std::vector<int32_t> gor, slen, gpar, plen;
+  int64_t saved = 0;
+};
+
+void group_requests(const Requests& q, uint32_t flags, Grouping* out) {
+  const auto h = cumulative_hashes(q);
+  const Trie t = build_trie(q, h);
+  const Levels L = build_levels(q, t);
+  out->gor.assign((size_t)q.R, -1);
+  out->slen.assign((size_t)q.R, 0);
+  out->gpar.clear();
+  out->plen.clear();
+  const int32_t chunk = q.chunk;
+  if (flags & PSATTN_FOREST_SINGLE) {
+    std::vector<int32_t> keep;
+    out->saved = single_level(L, &keep, L.deepest) * chunk;
+    // groups: the levels that keep two or more requests, in level order
+    std::vector<int32_t> gid(L.lv.size(), -1);
+    for (int32_t r = 0; r < q.R; ++r)
+      if (keep[r] >= 0) gid[keep[r]] = 0;
+    for (size_t v = 0; v < L.lv.size(); ++v)
+      if (gid[v] == 0) {
+        gid[v] = (int32_t)out->plen.size();
+        out->gpar.push_back(-1);
+        out->plen.push_back(L.lv[v].end_depth * chunk);
+      }
+    for (int32_t r = 0; r < q.R; ++r) {
+      const int32_t v = keep[r];
+      out->gor[r] = v >= 0 ? gid[v] : -1;
+      out->slen[r] = (int32_t)(q.len(r) - (v >= 0 ? (int64_t)L.lv[v].end_depth * chunk : 0));
+    }
+    return;
+  }
+  out->saved = 0;
+  for (const auto& lv : L.lv) {
+    out->saved += (int64_t)(lv.count - 1) * lv.chunks * chunk;
+    out->gpar.push_back(lv.parent);
+    out->plen.push_back(lv.chunks * chunk);
+  }
+  for (int32_t r = 0; r < q.R; ++r) {
+    const int32_t v = L.deepest[r];
+    out->gor[r] = v;
+    out->slen[r] = (int32_t)(q.len(r) - (v >= 0 ? (int64_t)L.lv[v].end_depth * chunk : 0));
+  }
+}
+
 }  // namespace
 
 extern "C" {
@@ -387,48 +437,83 @@ int psattn_forest_group(const int32_t* tokens, const int64_t* offsets, int32_t n
     return PSATTN_ERR_INVALID_ARG;
   const Requests q{tokens, offsets, num_req, chunk};
   try {
-    const auto h = cumulative_hashes(q);
-    const Trie t = build_trie(q, h);
-    const Levels L = build_levels(q, t);
-    if (flags & PSATTN_FOREST_SINGLE) {
-      std::vector<int32_t> keep;
-      const int64_t best = single_level(L, &keep, L.deepest);
-      // groups: the levels that keep two or more requests, in level order
-      std::vector<int32_t> gid(L.lv.size(), -1);
-      int32_t ng = 0;
-      for (int32_t r = 0; r < num_req; ++r)
-        if (keep[r] >= 0) gid[keep[r]] = 0;
-      for (size_t v = 0; v < L.lv.size(); ++v)
-        if (gid[v] == 0) gid[v] = ng++;
-      *num_groups = ng;
-      if (saved_tokens) *saved_tokens = best * chunk;
-      if (ng > cap) return PSATTN_ERR_NOMEM;
-      for (size_t v = 0; v < L.lv.size(); ++v)
-        if (gid[v] >= 0) {
-          group_parent[gid[v]] = -1;
-          prefix_len[gid[v]] = L.lv[v].end_depth * chunk;
-        }
-      for (int32_t r = 0; r < num_req; ++r) {
-        const int32_t v = keep[r];
-        group_of_req[r] = v >= 0 ? gid[v] : -1;
-        suffix_len[r] = (int32_t)(q.len(r) - (v >= 0 ? (int64_t)L.lv[v].end_depth * chunk : 0));
-      }
-      return PSATTN_OK;
-    }
-    const int32_t ng = (int32_t)L.lv.size();
+    Grouping gr;
+    group_requests(q, flags, &gr);
+    const int32_t ng = (int32_t)gr.plen.size();
     *num_groups = ng;
+    if (saved_tokens) *saved_tokens = gr.saved;
+    if (ng > cap) return PSATTN_ERR_NOMEM;
+    for (int32_t v = 0; v < ng; ++v) {
+      group_parent[v] = gr.gpar[v];
+      prefix_len[v] = gr.plen[v];
+    }
+    for (int32_t r = 0; r < num_req; ++r) {
+      group_of_req[r] = gr.gor[r];
+      suffix_len[r] = gr.slen[r];
+    }
+    return PSATTN_OK;
+  } catch (...) {
+    return PSATTN_ERR_NOMEM;
+  }
+}
+
+int psattn_cht_group(const int32_t* tokens, const int64_t* offsets, int32_t num_req,
+                     int32_t chunk, int32_t max_batch, int32_t max_new_chunks, uint32_t flags,
+                     int32_t* batch_of_req, int32_t* order, int32_t* num_batches,
+                     int32_t* batch_group_offset, int32_t* group_of_req, int32_t* group_parent,
+                     int32_t* prefix_len, int32_t* suffix_len, int32_t cap, int32_t* num_groups,
+                     int64_t* saved_tokens) {
+  if (!valid(tokens, offsets, num_req, chunk) || !num_batches || !num_groups ||
+      max_batch < 1 || max_new_chunks < 0 || cap < 0 || !batch_group_offset ||
+      (num_req > 0 && (!batch_of_req || !order || !group_of_req || !suffix_len)) ||
+      (cap > 0 && (!group_parent || !prefix_len)) || (flags & ~PSATTN_FOREST_SINGLE))
+    return PSATTN_ERR_INVALID_ARG;
+  const Requests q{tokens, offsets, num_req, chunk};
+  try {
+    const auto h = cumulative_hashes(q);
+    int32_t nb = 0;
+    cht_batches(q, h, max_batch, max_new_chunks, batch_of_req, order, &nb);
+    *num_batches = nb;
+    // each batch's requests in increasing id order
+    std::vector<std::vector<int32_t>> members((size_t)nb);
+    for (int32_t r = 0; r < num_req; ++r) members[batch_of_req[r]].push_back(r);
+    std::vector<int32_t> gpar_all, plen_all;
     int64_t saved = 0;
-    for (const auto& lv : L.lv) saved += (int64_t)(lv.count - 1) * lv.chunks * chunk;
+    batch_group_offset[0] = 0;
+    std::vector<int32_t> btok;
+    std::vector<int64_t> boff;
+    for (int32_t b = 0; b < nb; ++b) {
+      // the batch's token ids back to back
+      const std::vector<int32_t>& m = members[b];
+      btok.clear();
+      boff.assign(1, 0);
+      for (int32_t r : m) {
+        btok.insert(btok.end(), tokens + offsets[r], tokens + offsets[r + 1]);
+        boff.push_back((int64_t)btok.size());
+      }
+      if (btok.empty()) btok.push_back(0);
+      const Requests sub{btok.data(), boff.data(), (int32_t)m.size(), chunk};
+      Grouping gr;
+      group_requests(sub, flags, &gr);
+      const int32_t base = (int32_t)plen_all.size();
+      for (size_t v = 0; v < gr.plen.size(); ++v) {
+        gpar_all.push_back(gr.gpar[v] >= 0 ? base + gr.gpar[v] : -1);
+        plen_all.push_back(gr.plen[v]);
+      }
+      for (size_t i = 0; i < m.size(); ++i) {
+        group_of_req[m[i]] = gr.gor[i] >= 0 ? base + gr.gor[i] : -1;
+        suffix_len[m[i]] = gr.slen[i];
+      }
+      saved += gr.saved;
+      batch_group_offset[b + 1] = (int32_t)plen_all.size();
+    }
+    const int32_t ng = (int32_t)plen_all.size();
+    *num_groups = ng;
     if (saved_tokens) *saved_tokens = saved;
     if (ng > cap) return PSATTN_ERR_NOMEM;
     for (int32_t v = 0; v < ng; ++v) {
-      group_parent[v] = L.lv[v].parent;
-      prefix_len[v] = L.lv[v].chunks * chunk;
-    }
-    for (int32_t r = 0; r < num_req; ++r) {
-      const int32_t v = L.deepest[r];
-      group_of_req[r] = v;
-      suffix_len[r] = (int32_t)(q.len(r) - (v >= 0 ? (int64_t)L.lv[v].end_depth * chunk : 0));
+      group_parent[v] = gpar_all[v];
+      prefix_len[v] = plen_all[v];
     }
     return PSATTN_OK;
   } catch (...) {

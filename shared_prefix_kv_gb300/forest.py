@@ -15,7 +15,7 @@ from . import _lib, PsattnError
 
 FOREST_SINGLE = 1
 
-EXPORTED_SYMBOLS = ("psattn_forest_group", "psattn_cht_batches")
+EXPORTED_SYMBOLS = ("psattn_forest_group", "psattn_cht_batches", "psattn_cht_group")
 
 _vp = ctypes.c_void_p
 _lib.psattn_forest_group.argtypes = [_vp, _vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_uint32,
@@ -24,6 +24,10 @@ _lib.psattn_forest_group.restype = ctypes.c_int
 _lib.psattn_cht_batches.argtypes = [_vp, _vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                     ctypes.c_int32, _vp, _vp, _vp]
 _lib.psattn_cht_batches.restype = ctypes.c_int
+_lib.psattn_cht_group.argtypes = [_vp, _vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                  ctypes.c_int32, ctypes.c_uint32, _vp, _vp, _vp, _vp, _vp, _vp,
+                                  _vp, _vp, ctypes.c_int32, _vp, _vp]
+_lib.psattn_cht_group.restype = ctypes.c_int
 
 
 def pack(requests: Sequence[Sequence[int]]):
@@ -83,3 +87,43 @@ def cht_batches(requests=None, chunk: int = 16, max_batch: int = 64, max_new_chu
     if rc != 0:
         raise PsattnError(rc, "psattn_cht_batches")
     return bor[:R].copy(), order[:R].copy(), int(nb.value)
+
+
+def cht_group(requests=None, chunk: int = 16, max_batch: int = 64, max_new_chunks: int = 0,
+              single: bool = False, tokens=None, offsets=None):
+    """psattn_cht_group: CHT batches, each with its own group forest.  Returns
+    dict(batch_of_req, order, num_batches, batch_group_offset, group_of_req,
+    group_parent, prefix_len, suffix_len, saved_tokens), group ids global."""
+    tokens, offsets, R = _args(requests, tokens, offsets)
+    n = max(R, 1)
+    bor, order = np.zeros(n, np.int32), np.zeros(n, np.int32)
+    bgo = np.zeros(R + 1, np.int32)
+    gor, slen = np.zeros(n, np.int32), np.zeros(n, np.int32)
+    gpar, plen = np.zeros(n, np.int32), np.zeros(n, np.int32)
+    nb, ng, saved = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_int64(0)
+    rc = _lib.psattn_cht_group(tokens.ctypes.data, offsets.ctypes.data, R, int(chunk),
+                               int(max_batch), int(max_new_chunks),
+                               FOREST_SINGLE if single else 0, bor.ctypes.data,
+                               order.ctypes.data, ctypes.addressof(nb), bgo.ctypes.data,
+                               gor.ctypes.data, gpar.ctypes.data, plen.ctypes.data,
+                               slen.ctypes.data, n, ctypes.addressof(ng), ctypes.addressof(saved))
+    if rc != 0:
+        raise PsattnError(rc, "psattn_cht_group")
+    b, g = nb.value, ng.value
+    return {"batch_of_req": bor[:R].copy(), "order": order[:R].copy(), "num_batches": b,
+            "batch_group_offset": bgo[:b + 1].copy(), "group_of_req": gor[:R].copy(),
+            "group_parent": gpar[:g].copy(), "prefix_len": plen[:g].copy(),
+            "suffix_len": slen[:R].copy(), "saved_tokens": int(saved.value)}
+
+
+def batch_grouping(res, b):
+    """Batch b of a cht_group result as a batch of its own: (request ids,
+    group_of_req, group_parent, prefix_len, suffix_len) with group ids local
+    to the batch, ready for psattn_plan."""
+    lo, hi = int(res["batch_group_offset"][b]), int(res["batch_group_offset"][b + 1])
+    req = np.nonzero(res["batch_of_req"] == b)[0]
+    gor = res["group_of_req"][req].astype(np.int32)
+    gor = np.where(gor >= 0, gor - lo, -1).astype(np.int32)
+    gpar = res["group_parent"][lo:hi]
+    gpar = np.where(gpar >= 0, gpar - lo, -1).astype(np.int32)
+    return req, gor, gpar, res["prefix_len"][lo:hi].copy(), res["suffix_len"][req].copy()

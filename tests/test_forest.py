@@ -248,6 +248,64 @@ def test_cht_batches_match_brute_force(seed):
     assert nb == exp_n and bor.tolist() == exp_b and order.tolist() == exp_o
 
 
+@pytest.mark.parametrize("seed", range(30))
+@pytest.mark.parametrize("single", [False, True])
+def test_cht_group_matches_brute_force(seed, single):
+    """CHT batches with grouping metadata: the batches are those of the CHT
+    batch former (checked above against its brute-force simulation), and
+    within every batch the groups satisfy the longest-common-prefix checks
+    written from the definition (multi-level), or reach the exhaustive
+    optimum of first-level reuse (single level), on that batch alone."""
+    rng = np.random.default_rng(3000 + seed)
+    chunk = int(rng.integers(1, 3))
+    reqs = random_batch(rng, int(rng.integers(1, 12)), chunk, max_chunks=3 if single else 5)
+    max_batch = int(rng.integers(1, 6))
+    max_new = int(rng.integers(0, 4))
+    res = F.cht_group(reqs, chunk=chunk, max_batch=max_batch, max_new_chunks=max_new,
+                      single=single)
+    exp_b, exp_o, exp_n = brute_cht(reqs, chunk, max_batch, max_new)
+    assert res["num_batches"] == exp_n and res["batch_of_req"].tolist() == exp_b
+    assert res["order"].tolist() == exp_o
+    bgo = res["batch_group_offset"]
+    assert bgo[0] == 0 and bgo[-1] == len(res["prefix_len"]) and (np.diff(bgo) >= 0).all()
+    saved = 0
+    for b in range(exp_n):
+        req, gor, gpar, plen, slen = F.batch_grouping(res, b)
+        sub = [reqs[r] for r in req]
+        local = {"group_of_req": gor, "group_parent": None if single else gpar,
+                 "prefix_len": plen, "suffix_len": slen}
+        if single:
+            assert (gpar == -1).all()
+            # every group: members share its prefix; saving = exhaustive optimum
+            got = 0
+            for g, p in enumerate(plen):
+                m = [i for i in range(len(sub)) if gor[i] == g]
+                assert len(m) >= 2 and all(list(sub[i][:p]) == list(sub[m[0]][:p]) for i in m)
+                got += (len(m) - 1) * int(p)
+            assert got == brute_single(sub, chunk)
+            saved += got
+        else:
+            ch = chains(local)
+            for i in range(len(sub)):
+                depth = sum(int(plen[g]) for g in ch[i])
+                best = max([lcp_chunks(sub[i], sub[j], chunk) for j in range(len(sub)) if j != i]
+                           or [0])
+                assert depth == best * chunk
+                for j in range(i + 1, len(sub)):
+                    common = sum(int(plen[g]) for g in set(ch[i]) & set(ch[j]))
+                    assert common == lcp_chunks(sub[i], sub[j], chunk) * chunk
+            through = [sum(1 for c in ch if g in c) for g in range(len(plen))]
+            saved += sum((through[g] - 1) * int(plen[g]) for g in range(len(plen)))
+        for i, r in enumerate(req):
+            g = int(gor[i])
+            dep = 0
+            while g >= 0:
+                dep += int(plen[g])
+                g = int(gpar[g])
+            assert slen[i] == len(reqs[r]) - dep
+    assert res["saved_tokens"] == saved
+
+
 def test_forest_scales():
     # 2000 requests under 16 system prompts with 4 few-shot variants each
     rng = np.random.default_rng(7)

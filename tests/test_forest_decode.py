@@ -73,3 +73,30 @@ def test_decode_on_forest_groups(single):
     t_out, t_lse = tolerances(p)
     assert np.abs(out - o_ref).max() <= t_out
     assert np.abs(lse - l_ref).max() <= t_lse
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("single", [False, True])
+def test_decode_on_cht_batches(single):
+    """Feather's chunked-hash-tree batches, each grouped into prefix levels
+    (psattn_cht_group) and run through the planner and the fused decode as a
+    batch of its own, against the oracle."""
+    pytest.importorskip("torch")
+    from workloads.device import DeviceProblem, tolerances
+    reqs = token_batch(13, R=72)
+    res = F.cht_group(reqs, chunk=16, max_batch=24, max_new_chunks=4, single=single)
+    assert res["num_batches"] >= 3
+    for b in range(res["num_batches"]):
+        req, gor, gpar, plen, slen = F.batch_grouping(res, b)
+        part = {"group_of_req": gor, "group_parent": None if single else gpar,
+                "prefix_len": plen, "suffix_len": slen}
+        p = problem(part, seed=100 + b)
+        d = DeviceProblem(p)
+        with d.plan() as pl:
+            d.decode(pl)
+            out, lse = d.result()
+            assert pl.status() == (0, 0)
+        o_ref, l_ref = oracle.attention(p)
+        t_out, t_lse = tolerances(p)
+        assert np.abs(out - o_ref).max() <= t_out, b
+        assert np.abs(lse - l_ref).max() <= t_lse, b

@@ -125,6 +125,15 @@ def test_grouping_and_scheduling_calls_return_a_status():
             outcomes.add("cht ok")
         except ps.PsattnError as e:
             assert e.status == ps.ERR_INVALID_ARG, (it, e.status)
+        try:
+            c = F.cht_group(reqs, chunk=chunk, max_batch=int(rng.choice([1, 4, 64] + ext)),
+                            max_new_chunks=int(rng.choice([0, 1, 5] + ext)),
+                            single=bool(rng.random() < 0.5))
+            outcomes.add("cht group ok")
+            assert len(c["group_of_req"]) == len(reqs)
+            assert c["batch_group_offset"][-1] == len(c["prefix_len"])
+        except ps.PsattnError as e:
+            assert e.status == ps.ERR_INVALID_ARG, (it, e.status)
         R, NG = len(reqs), int(rng.integers(0, 6))
         gp = rng.integers(0, 300, size=NG)
         gor = rng.integers(-1, NG, size=R) if NG else -np.ones(R, np.int64)
@@ -140,4 +149,4 @@ def test_grouping_and_scheduling_calls_return_a_status():
             outcomes.add("sched ok")
         except ps.PsattnError as e:
             assert e.status == ps.ERR_INVALID_ARG, (it, e.status)
-    assert outcomes == {"forest ok", "cht ok", "sched ok"}
+    assert outcomes == {"forest ok", "cht ok", "cht group ok", "sched ok"}
