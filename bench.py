@@ -151,7 +151,10 @@ class ClockSampler:
             out, _ = self.proc.communicate(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-            out, _ = self.proc.communicate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:  # a sampler stuck in the driver: no samples
+                out = ""
         for line in out.splitlines():
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 7:
@@ -341,6 +344,7 @@ def per_workload(torch, ps, local, flush, min_launches=50, min_seconds=0.4, reus
             else:
                 cache = {wl: _make_named(wl)}  # one workload's inputs held at a time
         p, chunk_info = cache[wl]
+        print(f"per_workload: {label}", file=sys.stderr, flush=True)
         flags = 0
         for f in flag_names:
             flags |= getattr(ps, f)
@@ -353,7 +357,7 @@ def per_workload(torch, ps, local, flush, min_launches=50, min_seconds=0.4, reus
             d.decode(pl, stream)
         est = float(np.mean(timed(d, pl, 5)))
         n = int(max(min_launches, min(4000, math.ceil(min_seconds * 1e3 / (est + 0.05)))))
-        with ClockSampler(local, period_ms=20) as clk:
+        with ClockSampler(local, period_ms=50) as clk:
             times = timed(d, pl, n)
         rc, dflags = pl.status()
         ms = float(np.mean(times))

@@ -63,7 +63,7 @@ class PlanInfo(ctypes.Structure):
                 ("unique_kv_bytes", ctypes.c_int64), ("planned_kv_bytes", ctypes.c_int64),
                 ("qo_bytes", ctypes.c_int64), ("suffix_chunk_max", ctypes.c_int32),
                 ("prefix_chunk_max", ctypes.c_int32), ("num_sms", ctypes.c_int32),
-                ("grid", ctypes.c_int32)]
+                ("grid", ctypes.c_int32), ("dense_item_warps", ctypes.c_int32)]
 
 
 _vp = ctypes.c_void_p

@@ -85,6 +85,7 @@ struct HostPlan {
   int64_t unique_kv_bytes = 0, planned_kv_bytes = 0, qo_bytes = 0;
   int32_t suffix_chunk_max = 0, prefix_chunk_max = 0;
   int32_t any_ragged = 0;
+  int32_t dense_warps = 8;   // per-warp item warps that run beside the tensor-core items (4 or 8)
 };
 
 // Device-side view of a plan's workspace.
@@ -101,6 +102,7 @@ struct DevPlan {
   float2* mlpart;      // [slots][Hkv][G] (running max in log2 units, sum)
   int32_t n_witems, n_ditems;
   int32_t any_ragged;   // some request sees only part of its leaf level
+  int32_t dense_warps;  // per-warp item warps beside the tensor-core items (4 or 8)
 };
 
 }  // namespace psattn
