@@ -112,7 +112,7 @@ typedef struct {
     int32_t num_sms;          /* SM count the plan was sized for */
     int32_t grid;             /* CTAs psattn_decode launches */
     int32_t dense_item_warps; /* per-warp item warps per CTA that run beside the tensor-core
-                                 items (4 or 8; 0 without tensor-core items) */
+                                 items (4; 0 without tensor-core items) */
 } psattn_plan_info;
 
 /*

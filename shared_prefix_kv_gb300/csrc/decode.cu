@@ -39,22 +39,7 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-// Threads of the persistent CTA.  The CUDA-core paths run 12 warps, every
-// one on per-warp items.  The tensor-core path runs 16 warps in four
-// warpgroups whose register counts are moved between roles (setmaxnreg, see
-// the kernel): the launch gives each thread 128 registers.
-constexpr int kThreadsSimt = kWarpsPerCta * 32;
-constexpr int kThreadsMma = 16 * 32;
-constexpr int kMmaLaunchRegs = 128;   // kThreadsMma x 128 = the SM's 65536 registers
-constexpr int kRegsSoftmax = 152;     // warpgroup 0 during the dense items
-constexpr int kRegsControl = 40;      // warpgroup 1 during the dense items
-constexpr int kRegsItems = 160;       // per-warp item warpgroups
-constexpr int kRegsIdle = 32;         // warpgroup 0 once its dense items are done
-static_assert(kRegsSoftmax + kRegsControl + 2 * kRegsItems == 4 * kMmaLaunchRegs,
-              "register split during the dense items");
-static_assert(kRegsIdle + 3 * kRegsItems == 4 * kMmaLaunchRegs, "register split afterwards");
-template <int PATH>
-constexpr int threads_of() { return PATH == kPathMmaBf16D128 ? kThreadsMma : kThreadsSimt; }
+constexpr int kThreads = kWarpsPerCta * 32;
 
 struct Params {
   CUtensorMap kv_map;  // the pool as [num_blocks * 2 * Hkv * 16 rows][d] bf16, 128B swizzle
@@ -687,7 +672,7 @@ __device__ __forceinline__ void simt_item(const Params& P, const Item& it, int l
 //   warp 4      lane 0 issues the S = Q K^T MMAs and their commits;
 //   warps 5, 6  TMA producers of the K and the V tiles;
 //   warp 7      lane 0 issues the PV MMAs and their commits.
-// Warps 8-15 run per-warp items meanwhile (two per SM sub-partition).
+// Warps 8-11 run per-warp items meanwhile (one per SM sub-partition).
 //
 // For each 128-token tile g (counted across items, so the rings continue):
 //   TMA       K(g), V(g): 8 paged blocks x 2 halves of d, 128B-swizzled boxes
@@ -736,6 +721,7 @@ constexpr uint32_t kTmemP = 384;                        // two P buffers of 64 c
 #endif
 constexpr float kRescaleSumLimit = (float)(1u << PSATTN_RESCALE_LOG2_SUM);
 constexpr uint64_t kWaitLimitNs = 2000000000ull;        // 2 s per wait
+constexpr int kDenseThreads = 256;                      // warps 0-7
 
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -988,9 +974,30 @@ __device__ __forceinline__ int copy_width(int nrows) {
   return nrows <= 32 ? 32 : (nrows <= 64 ? 64 : kTileTok);
 }
 
-// TMA of one K or V tile into stage st: lane l < 16 copies the 16 x 64 box of
-// pool row `row` (a block's 16 tokens of one K|V head, -1 for none) into
-// its block's slot and half; lane 0 first posts the byte count.
+// Block-table lookup for the K or V tile of local tile j, by the 32 lanes of a
+// producer warp: lanes 0-15 each take one of the tile's 8 blocks (lane / 2)
+// and one 64-column half of it (lane % 2); returns the pool row of that block
+// half's 16 tokens, -1 for lanes without one (bad ids raise the error word
+// and are skipped).
+__device__ __forceinline__ int kv_row(const Params& P, const Span& s, int h, int kv, int j, int nb,
+                                      int lane) {
+  const int b = j * (kTileTok / kBlockSize) + (lane >> 1);
+  int row = -1;
+  if (lane < 16 && b < nb) {
+    const int col = s.col0 + b;
+    if (col >= P.maxb) {
+      raise(P, kErrColumn);
+    } else {
+      const int id = __ldg(&P.bt[(size_t)s.rep * P.maxb + col]);
+      if (id < 0 || id >= P.nblocks) raise(P, kErrBlockOob);
+      else row = ((id * 2 + kv) * P.Hkv + h) * kBlockSize;
+    }
+  }
+  return row;
+}
+
+// TMA of one K or V tile into stage st from the rows kv_row looked up; lane 0
+// first posts the byte count.
 __device__ __forceinline__ void issue_kv(const Params& P, const DenseState& d, int kv, uint32_t st,
                                          int row, int lane) {
   const uint32_t valid = __ballot_sync(0xffffffffu, row >= 0);
@@ -1018,7 +1025,7 @@ __device__ __forceinline__ void issue_kv(const Params& P, const DenseState& d, i
 // and the next completion needs an MMA it has not issued yet: K(g + 3) needs
 // kfree for S(g), sfree for S(g) needs S(g), V(g + 3) needs vfree for PV(g),
 // and P(g + 2) needs the softmax's wait for PV(g) (P buffer reuse).
-__device__ __forceinline__ void mma_s_item(const Params& P, DenseState& d, int ntiles) {
+__device__ void mma_s_item(const Params& P, DenseState& d, int ntiles) {
   if ((threadIdx.x & 31) != 0) return;
   const uint32_t g0 = d.g;
   const uint32_t idesc_s = idesc_bf16_m128_n128(false);
@@ -1039,7 +1046,7 @@ __device__ __forceinline__ void mma_s_item(const Params& P, DenseState& d, int n
   }
 }
 
-__device__ __forceinline__ void mma_pv_item(const Params& P, DenseState& d, int ntiles) {
+__device__ void mma_pv_item(const Params& P, DenseState& d, int ntiles) {
   if ((threadIdx.x & 31) != 0) return;
   const uint32_t g0 = d.g;
   const uint32_t idesc_o = idesc_bf16_m128_n128(true);
@@ -1061,12 +1068,10 @@ __device__ __forceinline__ void mma_pv_item(const Params& P, DenseState& d, int 
 // The producer warps' part of one item: warp 5 issues the K copies, warp 6
 // the V copies.  The first kStages tiles go straight into their stages (the
 // previous item is done with every stage); tile g >= kStages waits for the
-// stage's previous tile g - kStages to be consumed (kfree / vfree).  The
-// block ids come from a sliding window of 64 (two per lane, BlockWin): a
-// tile's 8 blocks lie in one half of it, and the next half is fetched four
-// tiles before it is needed, so no lookup latency sits on the path of a
-// tile's copies.
-__device__ __forceinline__ void producer_item(const Params& P, DenseState& d, const Span& s, int h, int kv, int nb,
+// stage's previous tile g - kStages to be consumed (kfree / vfree).  The block
+// ids of a tile are looked up before that wait, so the lookup's latency
+// overlaps it.
+__device__ void producer_item(const Params& P, DenseState& d, const Span& s, int h, int kv, int nb,
                               int ntiles) {
   const int lane = threadIdx.x & 31;
   const uint32_t g0 = d.g;
@@ -1075,20 +1080,9 @@ __device__ __forceinline__ void producer_item(const Params& P, DenseState& d, co
     if (lane == 0) ok = mbar_wait(bar, parity, d.abort);
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
   };
-  constexpr int kBpt = kTileTok / kBlockSize;  // blocks per tile (8: a quarter of a window half)
-  BlockWin win;
-  win.init(P, s, nb, lane);
   for (int j = 0; j < ntiles; ++j) {
     const uint32_t g = g0 + j, st = g % kStages;
-    const int b0 = j * kBpt;
-    win.advance(P, s, b0, nb, lane);
-    // lanes 0-15: block b0 + lane / 2, 64-column half lane % 2; the tile's
-    // blocks are all in the same half of the window (warp-uniform choice)
-    const int src = (b0 - win.base < 32) ? win.lo : win.hi;
-    const int id = __shfl_sync(0xffffffffu, src, (b0 + ((lane & 15) >> 1) - win.base) & 31);
-    const int row = (lane < 16 && b0 + (lane >> 1) < nb && id >= 0)
-                        ? ((id * 2 + kv) * P.Hkv + h) * kBlockSize
-                        : -1;
+    const int row = kv_row(P, s, h, kv, j, nb, lane);
     if (j >= kStages &&
         !wait0(kv ? bar_vfree(d, st) : bar_kfree(d, st), ((g / kStages) - 1) & 1))
       return;
@@ -1263,7 +1257,7 @@ __device__ __forceinline__ bool ring_wait(volatile uint32_t* e, bool want_empty)
 }
 
 // By lane 0 of a warp whose lanes acquired the unit's partials (its ticket).
-__device__ __forceinline__ bool mq_push(const Params& P, MergeRing& q, uint32_t unit) {
+__device__ bool mq_push(const Params& P, MergeRing& q, uint32_t unit) {
   if (atomicAdd(&q.count, 1) >= kMqCap) {
     atomicSub(&q.count, 1);
     return false;
@@ -1281,7 +1275,7 @@ __device__ __forceinline__ bool mq_push(const Params& P, MergeRing& q, uint32_t 
 
 // One unit from the ring, or -1 when it is empty (lane 0 claims, the warp gets
 // the answer).
-__device__ __forceinline__ int mq_pop(const Params& P, MergeRing& q, int lane) {
+__device__ int mq_pop(const Params& P, MergeRing& q, int lane) {
   int v = -1;
   if (lane == 0) {
     volatile int* cnt = &q.count;
@@ -1315,7 +1309,7 @@ __device__ __forceinline__ int mq_pop(const Params& P, MergeRing& q, int lane) {
 // d), one online-softmax step per partial; output bf16 (queued units come
 // only from tensor-core items).  (Loading several partials per step before
 // combining them made the whole launch about twice as slow.)
-__device__ __forceinline__ void merge_unit_body(const Params& P, int unit, int lane) {
+__device__ __noinline__ void merge_unit(const Params& P, int unit, int lane) {
   const int G = P.G, r = unit / P.Hkv, h = unit % P.Hkv;
   if (r < 0 || r >= P.R) {
     if (lane == 0) raise(P, kErrMerge);
@@ -1365,13 +1359,6 @@ __device__ __forceinline__ void merge_unit_body(const Params& P, int unit, int l
       if (P.lse) P.lse[(size_t)r * P.Hq + h * G + hl] = empty ? -INFINITY : (M + __log2f(L)) * kLn2;
     }
   }
-}
-
-// The same for the softmax warps (a full ring), out of line.  The per-warp
-// item warps inline it: a call out of a warpgroup whose register count was
-// raised would be compiled for the launch count.
-__device__ __noinline__ void merge_unit(const Params& P, int unit, int lane) {
-  merge_unit_body(P, unit, lane);
 }
 
 // The member tickets of the softmax warp's item, once its partial rows are
@@ -1550,9 +1537,7 @@ __device__ void softmax_item(const Params& P, DenseState& d, MergeRing& ring, co
   }
   // copy 0 (threads below cw) writes the row's partial.  A member whose
   // (request, KV head) unit has this one partial gets its output and LSE
-  // here instead: no partial slot, no ticket, no merge.  (Merging here with
-  // partials already in would put their loads on the tensor-core path: the
-  // merges stay with the per-warp item warps.)
+  // here instead: no partial slot, no ticket, no merge.
   const bool writer = tid < cw;
   float2* Y = reinterpret_cast<float2*>(d.smem + kOffV + 1024);  // [128]: the rows' m, l
   Y[tid] = make_float2(m_out, l_out);
@@ -1608,14 +1593,10 @@ __device__ void softmax_item(const Params& P, DenseState& d, MergeRing& ring, co
   settle_tickets(P, d, ring);
 }
 
-// Dense items of this CTA, run by warps 0-7 (256 threads): kSoftmax for
-// warpgroup 0 (Q gather, softmax, epilogue, TMEM allocation), else
-// warpgroup 1 (barrier set-up, the item claim, both MMA issuers and the two
-// TMA producers).  The two copies meet at the same dense_sync points.
-template <bool kSoftmax>
-__device__ __forceinline__ void dense_loop(const Params& P, uint8_t* smem_raw, MergeRing& ring) {
+// Dense items of this CTA, run by warps 0-7 (256 threads).
+__device__ void dense_loop(const Params& P, uint8_t* smem_raw, MergeRing& ring) {
   const int tid = threadIdx.x, warp = tid >> 5;
-  const bool control = !kSoftmax && tid == 128;
+  const bool control = (tid == 128);
   DenseState d;
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
@@ -1647,7 +1628,7 @@ __device__ __forceinline__ void dense_loop(const Params& P, uint8_t* smem_raw, M
     mbar_init(bar_x(d), 128);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (kSoftmax && warp == 0) {
+  if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(s_tmem)),
                  "r"(kTmemCols)
@@ -1679,12 +1660,12 @@ __device__ __forceinline__ void dense_loop(const Params& P, uint8_t* smem_raw, M
     const int nb = (ntok + kBlockSize - 1) / kBlockSize;
     const int ntiles = (ntok + kTileTok - 1) / kTileTok;
     int r_row = -1;
-    if (kSoftmax) r_row = prepare_item(P, d, it, nrows);
+    if (tid < 128) r_row = prepare_item(P, d, it, nrows);
     dense_sync();
-    if (kSoftmax) softmax_item(P, d, ring, it, s.t0, ntok, ntiles, nrows, r_row);
+    if (tid < 128) softmax_item(P, d, ring, it, s.t0, ntok, ntiles, nrows, r_row);
     else if (warp == 4) mma_s_item(P, d, ntiles);
     else if (warp == 7) mma_pv_item(P, d, ntiles);
-    else producer_item(P, d, s, it.kvh, warp - 5, nb, ntiles);
+    else if (warp == 5 || warp == 6) producer_item(P, d, s, it.kvh, warp - 5, nb, ntiles);
     tc_fence_before();
     dense_sync();
     d.g += ntiles;
@@ -1698,7 +1679,7 @@ __device__ __forceinline__ void dense_loop(const Params& P, uint8_t* smem_raw, M
   }
   tc_fence_before();
   dense_sync();
-  if (kSoftmax && warp == 0) {
+  if (warp == 0) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(d.tmem),
                  "r"(kTmemCols)
@@ -1727,14 +1708,29 @@ __device__ __forceinline__ void run_item(const Params& P, const Item& it, int la
   else simt_item<__nv_bfloat16, 128>(P, it, lane);
 }
 
-// Per-warp items until the list is empty; on the tensor-core path the
-// merges that tensor-core items queued in the CTA's ring are run between
-// items, and the ring is drained before the warp leaves.  Inlined into each
-// warpgroup that runs it (no calls out of line: see merge_unit).
 template <int PATH>
-__device__ __forceinline__ void item_loop(const Params& P, MergeRing& ring, volatile int* dense_active,
-                                          bool queue) {
+__global__ void __launch_bounds__(kThreads, 1) psattn_fused_decode(const __grid_constant__ Params P) {
   const int lane = threadIdx.x & 31;
+  // tensor-core items run (and may queue merges) while s_dense_active is set
+  __shared__ volatile int s_dense_active;
+  __shared__ MergeRing ring;
+  constexpr bool kMma = PATH == kPathMmaBf16D128;
+  const bool queue = kMma && P.dp.n_ditems > 0;
+  if constexpr (kMma) {
+    extern __shared__ uint8_t dyn_smem[];
+    if (queue) {
+      for (int i = threadIdx.x; i < kMqCap; i += blockDim.x) ring.e[i] = 0u;
+      if (threadIdx.x == 0) {
+        ring.count = ring.head = ring.tail = 0;
+        s_dense_active = 1;
+      }
+      __syncthreads();
+      if (threadIdx.x < kDenseThreads) {
+        dense_loop(P, dyn_smem, ring);
+        if (threadIdx.x == 0) s_dense_active = 0;
+      }
+    }
+  }
   for (;;) {
     int idx = 0;
     if (lane == 0) idx = (int)atomicAdd(&P.dp.ctr[kCtrWarp], 1u);
@@ -1745,8 +1741,7 @@ __device__ __forceinline__ void item_loop(const Params& P, MergeRing& ring, vola
     const Item it{a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
     run_item<PATH>(P, it, lane);
     if (queue) {  // the queued merges, between items
-      for (int u = mq_pop(P, ring, lane); u >= 0; u = mq_pop(P, ring, lane))
-        merge_unit_body(P, u, lane);
+      for (int u = mq_pop(P, ring, lane); u >= 0; u = mq_pop(P, ring, lane)) merge_unit(P, u, lane);
     }
   }
   if (queue) {
@@ -1756,11 +1751,11 @@ __device__ __forceinline__ void item_loop(const Params& P, MergeRing& ring, vola
     for (;;) {
       const int u = mq_pop(P, ring, lane);
       if (u >= 0) {
-        merge_unit_body(P, u, lane);
+        merge_unit(P, u, lane);
         t0 = global_ns();
         continue;
       }
-      if (!*dense_active) break;
+      if (!s_dense_active) break;
       if (global_ns() - t0 > kWaitLimitNs) {  // the CTA's tensor-core items never finished
         if (lane == 0) raise(P, kErrTimeout);
         break;
@@ -1768,26 +1763,6 @@ __device__ __forceinline__ void item_loop(const Params& P, MergeRing& ring, vola
       __nanosleep(1000);
     }
   }
-}
-
-// Register count of the calling warpgroup.  setmaxnreg is warpgroup-
-// collective and aligned: every thread of the four warps executes it, each
-// warp converged.  The lanes of the MMA-issuer and producer warps run apart
-// inside the dense loop, so every call reconverges its warp first.
-template <int N>
-__device__ __forceinline__ void regs_inc() {
-  __syncwarp();
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N) : "memory");
-}
-template <int N>
-__device__ __forceinline__ void regs_dec() {
-  __syncwarp();
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N) : "memory");
-}
-
-// End of the launch: every thread of the CTA has finished; the last CTA to
-// leave resets the work counters for the next launch.
-__device__ __forceinline__ void leave_cta(const Params& P) {
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
@@ -1799,89 +1774,8 @@ __device__ __forceinline__ void leave_cta(const Params& P) {
   }
 }
 
-// The tensor-core path: 16 warps in four warpgroups.
-//   warpgroup 0 (warps 0-3)   softmax and epilogue of the dense items at 152
-//                             registers, then 32 (idle);
-//   warpgroup 1 (warps 4-7)   the dense items' MMA issuers and TMA producers
-//                             at 40 registers, then per-warp items at 160;
-//   warpgroups 2, 3           per-warp items at 160 throughout.
-// The launch gives every thread 128; each raise is matched by lowering
-// elsewhere in the CTA (the sums are checked above), so every setmaxnreg.inc
-// is satisfied as soon as the matching setmaxnreg.dec has run.  With no dense
-// items, warpgroup 0 lowers to 32 and the other three raise to 160.  Each
-// warpgroup then leaves through its own copy of the end of the launch (its
-// own __syncthreads call site), so no code runs under two register counts.
-__device__ __forceinline__ void fused_mma(const Params& P, volatile int* dense_active, MergeRing& ring) {
-  extern __shared__ uint8_t dyn_smem[];
-  const int wg = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 7), 0);
-  const bool dense = P.dp.n_ditems > 0;
-  if (wg == 0) {
-    if (dense) {
-      regs_inc<kRegsSoftmax>();
-      dense_loop<true>(P, dyn_smem, ring);
-      if (threadIdx.x == 0) *dense_active = 0;
-    }
-    regs_dec<kRegsIdle>();
-    leave_cta(P);
-  } else if (wg == 1) {
-    if (dense) {
-      regs_dec<kRegsControl>();
-      dense_loop<false>(P, dyn_smem, ring);
-    }
-    regs_inc<kRegsItems>();
-    item_loop<kPathMmaBf16D128>(P, ring, dense_active, dense);
-    leave_cta(P);
-  } else {
-    regs_inc<kRegsItems>();
-    if (wg == 3 && dense && P.dp.dense_warps <= 4) {
-      // the plan runs four item warps beside the tensor-core items: this
-      // warpgroup joins once they are done (or after the wait limit)
-      const uint64_t t0 = global_ns();
-      while (*dense_active && global_ns() - t0 < kWaitLimitNs) __nanosleep(2000);
-    }
-    item_loop<kPathMmaBf16D128>(P, ring, dense_active, dense);
-    leave_cta(P);
-  }
-}
-
-template <int PATH>
-__global__ void __launch_bounds__(threads_of<PATH>(), 1) psattn_fused_decode(const __grid_constant__ Params P) {
-  // tensor-core items run (and may queue merges) while s_dense_active is set
-  __shared__ volatile int s_dense_active;
-  __shared__ MergeRing ring;
-  if constexpr (PATH == kPathMmaBf16D128) {
-    for (int i = threadIdx.x; i < kMqCap; i += blockDim.x) ring.e[i] = 0u;
-    if (threadIdx.x == 0) {
-      ring.count = ring.head = ring.tail = 0;
-      s_dense_active = P.dp.n_ditems > 0;
-    }
-    __syncthreads();
-    fused_mma(P, &s_dense_active, ring);
-  } else {
-    item_loop<PATH>(P, ring, &s_dense_active, false);
-    leave_cta(P);
-  }
-}
-
 template <int PATH>
 cudaError_t launch(const Params& P, int grid, cudaStream_t st) {
-  if constexpr (PATH == kPathMmaBf16D128) {
-    // The warpgroups' register split adds up only if the launch gives each
-    // thread exactly kMmaLaunchRegs: with fewer, a raise would wait for
-    // registers that are never freed.  Checked once per process.
-    static std::atomic<int> regs_ok{0};  // 0 unknown, 1 ok, -1 wrong
-    int ok = regs_ok.load(std::memory_order_acquire);
-    if (ok == 0) {
-      cudaFuncAttributes fa;
-      if (cudaFuncGetAttributes(&fa, psattn_fused_decode<PATH>) != cudaSuccess) {
-        cudaGetLastError();
-        return cudaErrorInvalidDeviceFunction;
-      }
-      ok = (fa.numRegs == kMmaLaunchRegs && fa.maxThreadsPerBlock >= kThreadsMma) ? 1 : -1;
-      regs_ok.store(ok, std::memory_order_release);
-    }
-    if (ok != 1) return cudaErrorInvalidConfiguration;
-  }
   const uint32_t smem = (PATH == kPathMmaBf16D128 && P.dp.n_ditems > 0) ? kDenseSmemBytes : 0;
   if (smem) {
     // the attribute is set once per device the process launches on (it holds
@@ -1898,7 +1792,7 @@ cudaError_t launch(const Params& P, int grid, cudaStream_t st) {
       if (dev >= 0 && dev < kMaxDevices) attr_set[dev].store(true, std::memory_order_release);
     }
   }
-  psattn_fused_decode<PATH><<<grid, threads_of<PATH>(), smem, st>>>(P);
+  psattn_fused_decode<PATH><<<grid, kThreads, smem, st>>>(P);
   return cudaGetLastError();
 }
 

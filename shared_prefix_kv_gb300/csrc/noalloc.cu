@@ -185,7 +185,6 @@ extern "C" int psattn_decode_noalloc(psattn_plan_t plan, const void* q, const vo
   dp.n_witems = (int32_t)hp.witems.size();
   dp.n_ditems = (int32_t)hp.ditems.size();
   dp.any_ragged = hp.any_ragged;
-  dp.dense_warps = hp.dense_warps;
   return psattn_launch_decode(hp, dp, q, kv_pool, block_table, group_of_req, prefix_len,
                               suffix_len, out, lse, stream);
 }

@@ -404,23 +404,6 @@ int build(const Inputs& in, int32_t num_sms, HostPlan& hp) {
   hp.planned_kv_bytes = planned_tok * tb;
   hp.qo_bytes = (int64_t)R * s.num_q_heads *
                 (2LL * s.head_dim * (s.dtype == PSATTN_F32 ? 4 : 2) + 4);
-
-  // Per-warp item warps beside the tensor-core items: 8 when the warp items
-  // would otherwise outlast the tensor-core phase by far, else 4 (every one
-  // of them slows the tiles it shares the SM with).  Estimates in SM cycles,
-  // from per-tile, per-item and per-token costs measured on the tensor-core
-  // path: ~2800 cycles per 128-token tile, ~25000 per tensor-core item, ~230
-  // per (token, KV head) of a per-warp item with four such warps per SM.
-  // Measured: the long-prefix batch (ratio 1.4) runs faster with 4, the
-  // two-level, Llama-3-8B-shaped and skewed batches (ratio 2 and above) with 8.
-  {
-    int64_t tiles = 0, warp_tok = 0;
-    for (const Item& it : hp.ditems) tiles += (it.cost + kDenseTileTok - 1) / kDenseTileTok;
-    for (const Item& it : hp.witems) warp_tok += it.cost;  // one read per item, whatever its rows
-    const double dense_cyc = ((double)tiles * 2800.0 + (double)hp.ditems.size() * 25000.0) / num_sms;
-    const double warp_cyc = (double)warp_tok * 230.0 / (4.0 * num_sms);
-    hp.dense_warps = (hp.ditems.empty() || warp_cyc > 1.5 * dense_cyc) ? 8 : 4;
-  }
   return PSATTN_OK;
 }
 
@@ -500,7 +483,6 @@ int upload(psattn_plan_s* p, cudaStream_t stream) {
   dp.n_witems = (int32_t)hp.witems.size();
   dp.n_ditems = (int32_t)hp.ditems.size();
   dp.any_ragged = hp.any_ragged;
-  dp.dense_warps = hp.dense_warps;
   cudaError_t e = cudaMemsetAsync(base + o_ctr, 0, o_wi - o_ctr, stream);  // counters + tickets
   auto put = [&](size_t o, const void* src, size_t bytes) {
     if (e == cudaSuccess && bytes) e = cudaMemcpyAsync(base + o, src, bytes, cudaMemcpyHostToDevice, stream);
@@ -655,7 +637,7 @@ int psattn_plan_info_get(psattn_plan_t plan, psattn_plan_info* info) {
   info->prefix_chunk_max = hp.prefix_chunk_max;
   info->num_sms = hp.num_sms;
   info->grid = hp.grid;
-  info->dense_item_warps = hp.ditems.empty() ? 0 : hp.dense_warps;
+  info->dense_item_warps = hp.ditems.empty() ? 0 : kDenseItemWarps;
   return PSATTN_OK;
 }
 

@@ -16,6 +16,7 @@ namespace psattn {
 
 constexpr int kBlockSize = 16;       // tokens per KV block (the only size built)
 constexpr int kWarpsPerCta = 12;     // warps of the persistent CTA (one CTA per SM)
+constexpr int kDenseItemWarps = 4;   // per-warp item warps (8-11) beside the tensor-core items
 constexpr int kMmaRows = 8;          // q vectors one mma.sync warp item serves (n = 8)
 constexpr int kSimtRows = 4;         // q vectors one CUDA-core warp item serves
 constexpr int kDenseRows = 128;      // rows of one tensor-core prefix tile (UMMA M)
@@ -85,7 +86,6 @@ struct HostPlan {
   int64_t unique_kv_bytes = 0, planned_kv_bytes = 0, qo_bytes = 0;
   int32_t suffix_chunk_max = 0, prefix_chunk_max = 0;
   int32_t any_ragged = 0;
-  int32_t dense_warps = 8;   // per-warp item warps that run beside the tensor-core items (4 or 8)
 };
 
 // Device-side view of a plan's workspace.
@@ -102,7 +102,6 @@ struct DevPlan {
   float2* mlpart;      // [slots][Hkv][G] (running max in log2 units, sum)
   int32_t n_witems, n_ditems;
   int32_t any_ragged;   // some request sees only part of its leaf level
-  int32_t dense_warps;  // per-warp item warps beside the tensor-core items (4 or 8)
 };
 
 }  // namespace psattn
