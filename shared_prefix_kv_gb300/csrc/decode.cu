@@ -701,9 +701,12 @@ constexpr int kStages = 3;                              // K and V ring depth
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kTileBytes;                  // kStages K stages
 constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;  // kStages V stages
-// between items the K stages hold the epilogue's O staging, [128][128] fp32
+// between items the K stages hold the epilogue's O staging, [128][kERow]
+// fp32 (a row of 128 values and a 16-byte pad)
 constexpr uint32_t kOffE = kOffK;
-static_assert(128 * 128 * 4 <= kStages * kTileBytes, "O staging overruns the K stages");
+constexpr int kERow = 132;
+static_assert(128 * kERow * 4 <= kStages * kTileBytes, "O staging overruns the K stages");
+static_assert((kERow * 4) % 16 == 0, "bulk copies need 16-byte aligned staging rows");
 constexpr int kMaxDenseBlocks = 512;                    // chunk <= 8192 tokens
 constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;  // 21 mbarriers
 constexpr uint32_t kOffMisc = kOffBar + 168;
@@ -785,6 +788,24 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// One bulk copy of `bytes` (a multiple of 16) from shared to global memory
+// by the TMA engine; both addresses 16-byte aligned.  The shared source must
+// have been made visible to the async proxy (fence_proxy_async) first.
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+               "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
+}
+
+// Commits this thread's bulk copies and waits until they are complete (the
+// global writes done, the shared sources read); the writes are then ordered
+// before this thread's later generic-proxy operations.
+__device__ __forceinline__ void bulk_commit_and_wait() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // named barrier 1 over the 256 threads of warps 0-7 (the dense group)
@@ -1268,8 +1289,11 @@ __device__ bool mq_push(const Params& P, MergeRing& q, uint32_t unit) {
     raise(P, kErrTimeout);
     return true;  // (the unit is lost; the error word says so)
   }
-  __threadfence();  // the partials this thread acquired, before the entry
-  *e = unit + 1u;
+  // Release at CTA scope: the reader is a warp of this CTA, and the partials
+  // this warp acquired (gpu scope, through the ticket) come with the entry.
+  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32((const void*)e)),
+               "r"(unit + 1u)
+               : "memory");
   return true;
 }
 
@@ -1289,7 +1313,9 @@ __device__ int mq_pop(const Params& P, MergeRing& q, int lane) {
         const int pos = atomicAdd(&q.head, 1) & (kMqCap - 1);
         volatile uint32_t* e = &q.e[pos];
         if (ring_wait(e, false)) {
-          v = (int)*e - 1;
+          uint32_t x;  // acquire at CTA scope: the pusher's partials are visible
+          asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(x) : "r"(smem_u32((const void*)e)) : "memory");
+          v = (int)x - 1;
           *e = 0u;
         } else {
           raise(P, kErrTimeout);
@@ -1300,7 +1326,7 @@ __device__ int mq_pop(const Params& P, MergeRing& q, int lane) {
     }
   }
   v = __shfl_sync(0xffffffffu, v, 0);
-  if (v >= 0) __threadfence();  // with the pusher's fence: its partials are visible
+  __syncwarp();  // the whole warp is ordered after lane 0's acquire
   return v;
 }
 
@@ -1382,7 +1408,7 @@ __device__ void settle_tickets(const Params& P, DenseState& d, MergeRing& ring) 
   d.pend_valid = 0;
   d.pend_any = 0;
   const uint32_t lastmask = __ballot_sync(0xffffffffu, last);
-  if (lastmask) __threadfence();  // the acquiring lanes' view, for the whole warp
+  __syncwarp();  // the acquiring lanes' view, for lane 0's push and the whole warp
   for (uint32_t m = lastmask; m; m &= m - 1) {
     const int mu = __ffs(m) - 1;
     const uint32_t unit = __shfl_sync(0xffffffffu, d.pend_unit, mu);
@@ -1490,17 +1516,19 @@ __device__ void softmax_item(const Params& P, DenseState& d, MergeRing& ring, co
     tc_fence_after();
   }
 
-  // ---- epilogue.  O rows go through shared memory (the K stages are idle
-  // until the next item) so that each member's G rows leave as contiguous
-  // 512-byte rows, lanes across d.  E is [128][128] fp32 with float4 c of row
-  // t at position c ^ (t % 8): conflict-free for the row-per-thread writes
-  // and the row-at-a-time reads.
+  // ---- epilogue.  Each row leaves as one bulk copy (cp.async.bulk, run by
+  // the TMA engine) of a staging row in shared memory: 512 B of fp32 partial
+  // output, or 256 B of bf16 output for a (request, KV head) unit whose only
+  // partial this is.  E is [128][kERow] fp32 over the idle K stages, a row
+  // per thread; the 16-byte pad makes the row-per-thread accesses free of
+  // bank conflicts.
   const int G = P.G, h = it.kvh;
   float* E = reinterpret_cast<float*>(d.smem + kOffE);
+  float4* Erow = reinterpret_cast<float4*>(E + tid * kERow);
   fence_proxy_async();  // E overlays K stages the TMA and the tensor cores used
   // Row copies: the row's maximum over its copies, each copy's O and l
-  // scaled to it; copy 0's warps then write the sums (the V stages are idle
-  // and hold the exchange).
+  // scaled to it; copy 0's threads then add the copies' rows into theirs
+  // (the V stages are idle and hold the exchange).
   float fac = 1.f, m_out = m_run, l_out = l_run;
   float* X = reinterpret_cast<float*>(d.smem + kOffV);  // [2][128]: m, then scaled l
   const int rho = tid % cw;
@@ -1524,66 +1552,63 @@ __device__ void softmax_item(const Params& P, DenseState& d, MergeRing& ring, co
       for (int e = 0; e < 32; ++e) o[e] = 0.f;
     }
 #pragma unroll
-    for (int e = 0; e < 32; e += 4) {
-      const int c = q4 * 8 + (e >> 2);
-      *reinterpret_cast<float4*>(E + tid * 128 + ((c ^ (tid & 7)) << 2)) =
-          make_float4(o[e] * fac, o[e + 1] * fac, o[e + 2] * fac, o[e + 3] * fac);
-    }
+    for (int e = 0; e < 32; e += 4)
+      Erow[q4 * 8 + (e >> 2)] = make_float4(o[e] * fac, o[e + 1] * fac, o[e + 2] * fac, o[e + 3] * fac);
   }
   if (ncopy > 1) {
-    if (!softmax_threads_sync(d)) return;  // every copy's E rows and l written
+    if (!softmax_threads_sync(d)) return;  // every copy's rows and l written
     l_out = 0.f;
     for (int c = 0; c < ncopy; ++c) l_out += X[128 + rho + c * cw];
+    if (tid < cw) {
+      for (int j = 0; j < 32; ++j) {
+        float4 v = Erow[j];
+        for (int c = 1; c < ncopy; ++c) {
+          const float4 w = reinterpret_cast<const float4*>(E + (tid + c * cw) * kERow)[j];
+          v.x += w.x;
+          v.y += w.y;
+          v.z += w.z;
+          v.w += w.w;
+        }
+        Erow[j] = v;
+      }
+    }
   }
-  // copy 0 (threads below cw) writes the row's partial.  A member whose
-  // (request, KV head) unit has this one partial gets its output and LSE
-  // here instead: no partial slot, no ticket, no merge.
+  // copy 0's threads write their rows.  A row whose unit has this one partial
+  // gets its output and LSE here: no partial slot, no ticket, no merge.
+  // (Merging here with partials already in would put their loads on the
+  // tensor-core path: the merges stay with the per-warp item warps.)
   const bool writer = tid < cw;
-  float2* Y = reinterpret_cast<float2*>(d.smem + kOffV + 1024);  // [128]: the rows' m, l
-  Y[tid] = make_float2(m_out, l_out);
-  if (writer && tid < nrows && r_row >= 0 && np_row > 1)
-    __stcg(&P.dp.mlpart[(((size_t)sb_row + it.slot_j) * P.Hkv + h) * G + tid % G],
-           make_float2(m_out, l_out));
+  if (writer && tid < nrows && r_row >= 0) {
+    if (np_row > 1) {
+      const size_t prow = (((size_t)sb_row + it.slot_j) * P.Hkv + h) * G + tid % G;
+      __stcg(&P.dp.mlpart[prow], make_float2(m_out, l_out));
+      fence_proxy_async();
+      bulk_store(P.dp.opart + prow * 128, Erow, 128 * 4);
+    } else {
+      const bool empty = !(l_out > 0.f);
+      const float inv = empty ? 0.f : 1.f / l_out;
+      // bf16 in place: quad j (8 B) lands below float4 j, which is read first
+      uint2* Eb = reinterpret_cast<uint2*>(Erow);
+      for (int j = 0; j < 32; ++j) {
+        const float4 v = Erow[j];
+        Eb[j] = make_uint2(pack_bf16(v.x * inv, v.y * inv), pack_bf16(v.z * inv, v.w * inv));
+      }
+      const size_t orow = (size_t)r_row * P.Hq + h * G + tid % G;
+      if (empty) raise(P, kErrEmpty);
+      if (P.lse) P.lse[orow] = empty ? -INFINITY : (m_out + __log2f(l_out)) * kLn2;
+      fence_proxy_async();
+      bulk_store(reinterpret_cast<__nv_bfloat16*>(P.out) + orow * 128, Erow, 128 * 2);
+    }
+    // the row is in global memory (and its staging read) before the tickets
+    // below publish it and before the next item's K tiles land over E
+    bulk_commit_and_wait();
+  }
   tc_fence_before();
   __syncwarp();
   // this warp's members: lane mu speaks for member mu (rows warp * 32 + mu * G ..)
   const int mpw = 32 / G, src = (lane < mpw ? lane : 0) * G;
-  const int sb_m = __shfl_sync(0xffffffffu, sb_row, src);
   const int r_m = __shfl_sync(0xffffffffu, r_row, src);
   const int np_m = __shfl_sync(0xffffffffu, np_row, src);
-  for (int mu = 0; mu < mpw; ++mu) {
-    const int row0 = warp * 32 + mu * G;
-    if (row0 >= nrows || warp * 32 >= cw) break;
-    const int sbm = __shfl_sync(0xffffffffu, sb_m, mu);
-    const int rm = __shfl_sync(0xffffffffu, r_m, mu);
-    const bool only = __shfl_sync(0xffffffffu, np_m, mu) == 1;
-    float* dst = P.dp.opart + ((((size_t)sbm + it.slot_j) * P.Hkv + h) * G) * 128;
-    for (int x = lane; x < G * 32; x += 32) {
-      const int rr = x >> 5, c = x & 31, row = row0 + rr;
-      float4 v = *reinterpret_cast<const float4*>(E + row * 128 + ((c ^ (row & 7)) << 2));
-      for (int k = 1; k < ncopy; ++k) {
-        const int rk = row + k * cw;
-        const float4 w = *reinterpret_cast<const float4*>(E + rk * 128 + ((c ^ (rk & 7)) << 2));
-        v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
-      }
-      if (!only) {
-        __stcg(reinterpret_cast<float4*>(dst + rr * 128 + c * 4), v);
-        continue;
-      }
-      if (rm < 0) continue;
-      const float2 ml = Y[row];
-      const bool empty = !(ml.y > 0.f);
-      const float inv = empty ? 0.f : 1.f / ml.y;
-      const int hq = h * G + rr;
-      __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(P.out) + ((size_t)rm * P.Hq + hq) * 128;
-      *reinterpret_cast<uint2*>(o + c * 4) =
-          make_uint2(pack_bf16(v.x * inv, v.y * inv), pack_bf16(v.z * inv, v.w * inv));
-      if (c == 0) {
-        if (empty) raise(P, kErrEmpty);
-        if (P.lse) P.lse[(size_t)rm * P.Hq + hq] = empty ? -INFINITY : (ml.x + __log2f(ml.y)) * kLn2;
-      }
-    }
-  }
   // lane mu takes member mu's ticket (units with more than one partial); the
   // last arriver of a unit queues its merge
   d.pend_valid = writer && lane < mpw && warp * 32 + lane * G < nrows && r_m >= 0 && np_m > 1;
