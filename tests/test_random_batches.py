@@ -81,7 +81,7 @@ def test_random_plan_covers_every_token_once(seed):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("seed", range(150))
 def test_random_batches_gpu_parity(seed):
     shapes = [dict(), dict(Hq=16, Hkv=8), dict(dtype=W.F32, d=64, Hq=8, Hkv=2)]
     _gpu_parity(make_case(1000 + seed, **shapes[seed % 3]))
