@@ -344,7 +344,7 @@ def test_device_error_word_on_group_mismatch():
 FULL = ["tiny_fp32", "llama8b", "long_prefix", "skewed", "two_level", "two_level_flat"]
 
 
-def _sample(p, n=40):
+def _sample(p, n=160):
     rng = np.random.default_rng(11)
     picks = set(rng.choice(p.num_req, size=min(n, p.num_req), replace=False).tolist())
     picks.add(int(np.argmax(p.suffix_len)))
