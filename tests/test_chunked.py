@@ -61,7 +61,8 @@ def tiny_fp32_chunked():
     return p, ql, W.chunk_queries(p, ql)
 
 
-CASES = [("chunked", s) for s in (6, 7, 8)] + [("two_level", s) for s in (4, 9)]
+CASES = ([("chunked", s) for s in range(6, 16)] +
+         [("two_level", s) for s in (4, 9, 11, 13, 15, 17)])
 
 
 def make_case(kind, seed):
